@@ -1,0 +1,450 @@
+"""Benchmark: overlap-save FIR output throughput (GS/s) on GB300, with its roofline fraction.
+
+One step is one pass of the whole hot path -- the fused block kernel over one call's input
+(steps 3-5 of the overlap-save claim in "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法",
+zl.czvv.com/42398539.html, plus the state carry) -- for the chosen workload (default C2:
+complex64, k = 4096 blocks of L = 3073, M = 1024, N = 4096, one call).  The C4 workload's step
+is its stream of 64 calls.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun each rank filters its own copy of the workload
+on its own GPU (replicas, weak scaling; no data-path collective) and the time is the maximum
+over ranks.  `--impl reference` times the float64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "overlap-save FIR output GS/s on 1 GB300; % of HBM/FP32 roofline"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FP32_LANES_PER_SM = 128
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------------------- roofline arithmetic
+
+
+def bytes_per_output(w: W.Workload) -> float:
+    """Algorithmic HBM bytes per output sample: the gather reads N samples per L outputs
+    (input plus the (M-1)/L overlap re-read) and the store writes one."""
+    s = w.sample_bytes
+    return s * (1.0 + (w.M - 1) / w.L) + s
+
+
+def flops_per_output(w: W.Workload) -> float:
+    """Nominal flops per output sample: 5 N log2 N per complex N-point FFT (radix-2 count),
+    two transforms and a 6N-flop complex multiply per block of L outputs; a real block pair
+    shares one complex transform."""
+    per_block = 2 * 5 * w.N * math.log2(w.N) + 6 * w.N
+    return per_block / w.L / (2 if w.real else 1)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "frequency_domain_order_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """dram bytes per launch from a committed ncu summary for this workload, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(PROFILE_DIR, f"traffic_{config}.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None, d.get("source_hash")
+    return float(d["dram_bytes_per_launch"]), d.get("source_hash")
+
+
+# ----------------------------------------------------------------------------- clocks (NVML)
+
+_NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Reads SM clocks and clock-event reasons through NVML (read-only queries) every
+    `period` seconds on a background thread while the timed region runs."""
+
+    def __init__(self, device_index: int, period: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.period = period
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            bus = self._bus_id(device_index)
+            rc = -1
+            if bus:
+                rc = self.nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            return
+
+    @staticmethod
+    def _bus_id(idx):
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(idx)
+            return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            return None
+
+    def _read(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        f(self.h, ctypes.byref(rs))
+        return int(clk.value), int(rs.value)
+
+    def __enter__(self):
+        self._stop = threading.Event()
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def _run(self):
+        while not self._stop.is_set():
+            mhz, rs = self._read()
+            self.samples.append(mhz)
+            self.reasons |= rs
+            time.sleep(self.period)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples),
+                "reasons": [n for b, n in _NVML_REASONS.items() if self.reasons & b and b != 0x1],
+                "source": "NVML, sampled every 2 ms during the timed region"}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def config_block(w: W.Workload, footprint: int):
+    l2 = (f"inputs larger than L2: steps alternate between 2 input/output buffer sets, "
+          f"{footprint / 1e6:.0f} MB in total vs {L2_BYTES / 2**20:.0f} MiB L2") if footprint else \
+        "host CPU run (no GPU L2 involved)"
+    return {
+        "workload": f"{w.name}: {w.description}",
+        "n_samples": w.n, "calls_per_step": len(w.calls), "M": w.M, "N": w.N, "L": w.L,
+        "sample": "float32" if w.real else "complex64",
+        "coefficients": "H given (complex64)" if w.coef == "freq" else "h taps",
+        "l2": l2,
+    }
+
+
+def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
+    import torch
+
+    from frequency_domain_order_gb300 import build as fbuild
+    from frequency_domain_order_gb300 import fir_os
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or not os.path.exists(fbuild.LIB):
+        fbuild.build()
+    barrier(world)
+
+    x = W.make_x(w)
+    if w.coef == "freq":
+        coef = torch.from_numpy(W.make_H_given(w)).to(dev)
+        plan = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=fir_os.COEF_FREQ)
+    else:
+        coef = torch.from_numpy(W.make_h_device(w)).to(dev)
+        plan = fir_os.Plan(w.M, w.N, coef, real=w.real)
+    sets = 2
+    xs = [torch.from_numpy(x).to(dev) for _ in range(sets)]
+    ys = [torch.empty_like(xs[0]) for _ in range(sets)]
+    sts = [torch.zeros(w.M - 1, dtype=xs[0].dtype, device=dev) for _ in range(sets)]
+    footprint = sets * 2 * x.nbytes
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, evs=None):
+        k = i % sets
+        off = 0
+        for q, c in enumerate(w.calls):
+            if evs is not None:
+                evs[q][0].record(stream)
+            plan.execute(xs[k][off: off + c], ys[k][off: off + c], sts[k], stream)
+            if evs is not None:
+                evs[q][1].record(stream)
+            off += c
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    plan.device_status()
+
+    K = args.steps
+    ncall = len(w.calls)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(ncall)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for i in range(K):
+            step(i, ev[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    plan.device_status()
+    total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
+    # each call of a step is one launch of the block kernel (the state is written in-kernel)
+    launch_ms = statistics.fmean(a.elapsed_time(b) for step_ev in ev for a, b in step_ev)
+    ms_step = reduce_max(total_ms / K, world, dev)
+    launches_per_step = sum(plan.launches(c) for c in w.calls)
+
+    value = world * w.n / (ms_step * 1e-3) / 1e9
+    peak, peak_kind, peaks = measured_peaks()
+    bytes_step = w.n * bytes_per_output(w)
+    bytes_launch = bytes_step / ncall
+    achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
+    traffic, _ = profiled_traffic(w.name)
+    clk = clocks.summary()
+    sm_mhz = clk["sm_mhz"] if clk else (peaks.get("sm_max_mhz") or 2070.0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    flops_step = w.n * flops_per_output(w)
+    t_hbm = bytes_step / (peak * 1e9)
+    t_fp32 = flops_step / (fp32_peak * 1e12)
+
+    # end to end through the host-buffer entry point (pinned memory, copies in the timed region)
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    sh = torch.zeros(w.M - 1, dtype=xh.dtype).pin_memory()
+
+    def e2e_step():
+        off = 0
+        for c in w.calls:
+            plan.execute_host(xh[off: off + c], yh[off: off + c], sh, stream)
+            off += c
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, world, dev)
+    sb = w.sample_bytes
+    e2e = {"value": world * w.n / e2e_s / 1e9, "unit": "GS/s",
+           "h2d_bytes_per_step": w.n * sb + len(w.calls) * (w.M - 1) * sb,
+           "d2h_bytes_per_step": w.n * sb + len(w.calls) * (w.M - 1) * sb,
+           "steps": e2e_steps,
+           "path": "fir_os_execute_host: pinned host x -> device -> fused kernel -> pinned host y, "
+                   "chunks of ~2^21 samples pipelined over 3 streams"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "GS/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(w, footprint),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": bytes_launch,
+                     "kernel_ms_per_launch": launch_ms},
+        "fp32": {"nominal_flops_per_output": flops_per_output(w),
+                 "achieved_tflops": flops_step / ncall / (launch_ms * 1e-3) / 1e12,
+                 "peak_tflops": fp32_peak,
+                 "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_mhz:.0f} MHz (median sampled)",
+                 "frac": flops_step / ncall / (launch_ms * 1e-3) / 1e12 / fp32_peak},
+        "metric_roofline": {"t_hbm_us": t_hbm * 1e6, "t_fp32_us": t_fp32 * 1e6,
+                            "bound": "hbm" if t_hbm >= t_fp32 else "fp32",
+                            "frac": max(t_hbm, t_fp32) / (ms_step * 1e-3)},
+        "e2e": e2e,
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk,
+        "kernel": plan.kernel(),
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+    plan.close()
+    return out
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+
+def cpu_baseline(w: W.Workload, x, budget_s: float = 12.0):
+    """Time the float64 oracle (direct convolution, all host cores) on a bounded sample of
+    the workload: the first whole blocks of the stream, as many as fit the time budget."""
+    import oracle
+    h = W.oracle_h(w)
+    probe = min(w.n, max(w.L, 4096))
+    t0 = time.perf_counter()
+    oracle.direct_at(x, h, None, np.arange(probe, dtype=np.int64))
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    count = int(min(w.n, max(w.L, rate * budget_s)))
+    idx = np.arange(count, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.direct_at(x, h, None, idx)
+    dt = time.perf_counter() - t0
+    return {"value": count / dt / 1e9, "unit": "GS/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"first {count} of {w.n} outputs ({count / w.n:.1%}), float64 direct "
+                      f"convolution with M={w.M} taps, OpenMP over outputs"}
+
+
+def run_reference(args, w: W.Workload, world: int, rank: int):
+    """The oracle as the reference arm: each step evaluates a bounded contiguous sample of
+    outputs; the whole run is sized to end within a few minutes."""
+    if rank != 0:
+        return None
+    import oracle
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    probe = min(w.n, 2048)
+    t0 = time.perf_counter()
+    oracle.direct_at(x, h, None, np.arange(probe, dtype=np.int64))
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = min(0.5, 120.0 / max(1, args.steps + args.warmup))
+    count = int(max(64, min(w.n, rate * per_step_s)))
+    rng = np.random.Generator(np.random.PCG64(99))
+    starts = rng.integers(0, max(1, w.n - count), args.steps + args.warmup)
+    for i in range(args.warmup):
+        oracle.direct_at(x, h, None, np.arange(starts[i], starts[i] + count, dtype=np.int64))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = starts[args.warmup + i]
+        oracle.direct_at(x, h, None, np.arange(s, s + count, dtype=np.int64))
+    dt = (time.perf_counter() - t0) / args.steps
+    value = count / dt / 1e9
+    sample = (f"{count} contiguous outputs per step at seeded random offsets "
+              f"({count / w.n:.3%} of the {w.n}-sample stream), float64 direct convolution")
+    return {
+        "metric": METRIC, "value": value, "unit": "GS/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": config_block(w, 0),
+        "cpu_baseline": {"value": value, "unit": "GS/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GS/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    w = W.WORKLOADS[args.config]
+    if args.impl == "reference":
+        out = run_reference(args, w, world, rank)
+    else:
+        out = run_ours(args, w, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

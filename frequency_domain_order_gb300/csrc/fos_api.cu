@@ -1,0 +1,610 @@
+// fos_api.cu -- the C ABI of libfir_os.so (include/fir_os.h): plans, argument checks,
+// launches, the plan-time kernels and the pipelined host-buffer path.
+//
+// Method: "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法" (zl.czvv.com/42398539.html),
+// 主权项 steps 1-6.  Step 1 (frequency response) runs here at plan time; steps 3-5 run in the
+// fused block kernels (fos_block.cuh, fos_cluster.cu); steps 2 and 6 (moving chunks between
+// host and device and repeating) are fir_os_execute_host.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/fir_os.h"
+#include "fos_fft.cuh"
+#include "fos_kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(FIR_OS_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define FOS_CUDA(call, what)                          \
+    do {                                              \
+        cudaError_t e_ = (call);                      \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+// ------------------------------------------------------------------ plan-time kernels
+
+// A[t] = h[t] (t < M), 0 (M <= t < N), in float64.
+__global__ void fos_fill_h64(double2 *A, const void *h, int M, int N, int h_complex) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= N) return;
+    double2 v = make_double2(0.0, 0.0);
+    if (t < M) {
+        if (h_complex) {
+            const float2 z = static_cast<const float2 *>(h)[t];
+            v = make_double2((double)z.x, (double)z.y);
+        } else {
+            v = make_double2((double)static_cast<const float *>(h)[t], 0.0);
+        }
+    }
+    A[t] = v;
+}
+
+// One radix-2 Stockham pass of the forward float64 FFT: group j = 0..N/2-1 reads z[j] and
+// z[j + N/2], multiplies the second by e^{-2 pi i m / (2 Ns)} (m = j mod Ns) and writes the
+// sum and difference to (j / Ns) 2 Ns + m and that + Ns.
+__global__ void fos_radix2_pass64(const double2 *src, double2 *dst, int N, int Ns) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= N / 2) return;
+    const int m = j & (Ns - 1);
+    double s, c;
+    sincospi(-(double)m / (double)Ns, &s, &c);
+    const double2 a = src[j], b0 = src[j + N / 2];
+    const double2 b = make_double2(b0.x * c - b0.y * s, b0.x * s + b0.y * c);
+    const int o = (j / Ns) * 2 * Ns + m;
+    dst[o] = make_double2(a.x + b.x, a.y + b.y);
+    dst[o + Ns] = make_double2(a.x - b.x, a.y - b.y);
+}
+
+// H[t] = A[t] / N rounded to float32 (the inverse transform's 1/N folded into H).
+__global__ void fos_finish_h(const double2 *A, float2 *H, int N) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < N) H[t] = make_float2((float)(A[t].x / N), (float)(A[t].y / N));
+}
+
+// H[t] = Hin[t] / N (N a power of two: exact).
+__global__ void fos_scale_h(const float2 *Hin, float2 *H, int N) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < N) {
+        const float s = 1.0f / (float)N;
+        H[t] = make_float2(Hin[t].x * s, Hin[t].y * s);
+    }
+}
+
+// S0' = last M-1 samples of concat(S0, x), in place, one CTA.  Used when the block kernel
+// cannot write the state itself (more than one work unit reads S0).  For n < M-1 the kept
+// part of S0 moves towards the front; chunks are read completely before they are written and
+// every later chunk reads only indices beyond what earlier chunks wrote.
+template <typename T>
+__global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist) {
+    if (n >= hist) {
+        for (int t = threadIdx.x; t < hist; t += blockDim.x) state[t] = x[n - hist + t];
+        return;
+    }
+    const int keep = hist - (int)n;  // samples of S0 that stay
+    for (int c0 = 0; c0 < hist; c0 += blockDim.x) {
+        const int t = c0 + threadIdx.x;
+        T v{};
+        if (t < hist) v = t < keep ? state[n + t] : x[t - keep];
+        __syncthreads();
+        if (t < hist) state[t] = v;
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ plan
+
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+    if (na == 0 || nb == 0) return false;
+    return a < b + nb && b < a + na;
+}
+
+}  // namespace
+
+struct fir_os_plan {
+    int M = 0, N = 0, L = 0;
+    int data_kind = FIR_OS_COMPLEX;
+    int device = 0;
+    int sms = 0;
+    fos::KernelEntry kernel;
+    int max_units_in_flight = 0;  // CTAs (single-CTA kernel) or clusters (cluster kernel)
+    float2 *d_H = nullptr;
+    float2 *d_tw = nullptr;
+    float2 *d_twa = nullptr;
+    int *d_err = nullptr;
+    // host-buffer path (lazily created)
+    int64_t host_chunk = 0;
+    void *hx[2] = {nullptr, nullptr};
+    void *hy[2] = {nullptr, nullptr};
+    void *hstate = nullptr;
+    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
+    cudaEvent_t ev_start = nullptr;
+};
+
+namespace {
+
+int sample_bytes(const fir_os_plan *p) { return p->data_kind == FIR_OS_REAL ? 4 : 8; }
+
+void free_plan(fir_os_plan *p) {
+    if (!p) return;
+    cudaFree(p->d_H);
+    cudaFree(p->d_tw);
+    cudaFree(p->d_twa);
+    cudaFree(p->d_err);
+    for (int k = 0; k < 2; ++k) {
+        cudaFree(p->hx[k]);
+        cudaFree(p->hy[k]);
+        if (p->ev_in[k]) cudaEventDestroy(p->ev_in[k]);
+        if (p->ev_comp[k]) cudaEventDestroy(p->ev_comp[k]);
+        if (p->ev_out[k]) cudaEventDestroy(p->ev_out[k]);
+    }
+    cudaFree(p->hstate);
+    if (p->ev_start) cudaEventDestroy(p->ev_start);
+    if (p->s_in) cudaStreamDestroy(p->s_in);
+    if (p->s_comp) cudaStreamDestroy(p->s_comp);
+    if (p->s_out) cudaStreamDestroy(p->s_out);
+    delete p;
+}
+
+// Stockham pass twiddles of a 2^logn-point per-CTA transform (layout in fos_fft.cuh),
+// computed in float64 and rounded.
+template <int LOGN>
+void fill_pass_twiddles(std::vector<float2> &tw) {
+    using S = fos::FftShape<LOGN>;
+    tw.assign(S::TW_ENTRIES > 0 ? S::TW_ENTRIES : 1, make_float2(0.f, 0.f));
+    for (int p = 1; p < S::NPASS; ++p) {
+        const int Ns = S::ns(p);
+        const long long period = 16LL * Ns;
+        for (int r = 1; r < 16; ++r)
+            for (int m = 0; m < Ns; ++m) {
+                const long long e = ((long long)m * r) % period;
+                const double ang = -2.0 * M_PI * (double)e / (double)period;
+                tw[S::twoff(p) + (r - 1) * Ns + m] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+    }
+}
+
+bool pass_twiddles(int logn, std::vector<float2> &tw) {
+    switch (logn) {
+        case 6: fill_pass_twiddles<6>(tw); return true;
+        case 7: fill_pass_twiddles<7>(tw); return true;
+        case 8: fill_pass_twiddles<8>(tw); return true;
+        case 9: fill_pass_twiddles<9>(tw); return true;
+        case 10: fill_pass_twiddles<10>(tw); return true;
+        case 11: fill_pass_twiddles<11>(tw); return true;
+        case 12: fill_pass_twiddles<12>(tw); return true;
+        case 13: fill_pass_twiddles<13>(tw); return true;
+        default: return false;
+    }
+}
+
+int ilog2i(int v) {
+    int r = 0;
+    while ((1 << r) < v) ++r;
+    return r;
+}
+
+int64_t units_for(const fir_os_plan *p, int64_t n) {
+    const int64_t blocks = (n + p->L - 1) / p->L;
+    const int64_t per = p->data_kind == FIR_OS_REAL ? (blocks + 1) / 2 : blocks;  // transforms
+    return (per + p->kernel.units_per_cta - 1) / p->kernel.units_per_cta;
+}
+
+// The block kernel writes S0' itself when only its first work unit reads S0 (the next unit
+// starts at or after sample 0); the cluster kernel additionally needs n >= M-1, because its
+// copy of S0 is spread over the cluster's CTAs.
+bool fuse_state(const fir_os_plan *p, int64_t n) {
+    if (p->M == 1) return true;
+    const int64_t span = (int64_t)p->kernel.units_per_cta * p->L * (p->data_kind == FIR_OS_REAL ? 2 : 1);
+    if (p->kernel.cluster == 1) return span >= p->M - 1;
+    return span >= p->M - 1 && n >= p->M - 1;
+}
+
+int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state, cudaStream_t stream) {
+    const bool real = p->data_kind == FIR_OS_REAL;
+    fos::BlockParams bp{};
+    bp.x = x;
+    bp.y = y;
+    bp.state = state;
+    bp.H = p->d_H;
+    bp.tw = p->d_tw;
+    bp.twa = p->d_twa;
+    bp.err = p->d_err;
+    bp.n = n;
+    bp.nunits = units_for(p, n);
+    bp.M = p->M;
+    bp.L = p->L;
+    bp.fuse_state = fuse_state(p, n);
+    const int64_t groups = bp.nunits < p->max_units_in_flight ? bp.nunits : p->max_units_in_flight;
+    void *args[] = {&bp};
+    if (p->kernel.cluster == 1) {
+        FOS_CUDA(cudaLaunchKernel(p->kernel.func, dim3((unsigned)groups), dim3(p->kernel.threads), args,
+                                  (size_t)p->kernel.smem, stream),
+                 "block kernel launch");
+    } else {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)(groups * p->kernel.cluster));
+        cfg.blockDim = dim3(p->kernel.threads);
+        cfg.dynamicSmemBytes = (size_t)p->kernel.smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = p->kernel.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        FOS_CUDA(cudaLaunchKernelExC(&cfg, p->kernel.func, args), "cluster kernel launch");
+    }
+    if (!bp.fuse_state && p->M > 1) {
+        if (real)
+            fos_state_kernel<float><<<1, 1024, 0, stream>>>(static_cast<const float *>(x), n,
+                                                            static_cast<float *>(state), p->M - 1);
+        else
+            fos_state_kernel<float2><<<1, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
+                                                             static_cast<float2 *>(state), p->M - 1);
+        FOS_CUDA(cudaGetLastError(), "state kernel launch");
+    }
+    return FIR_OS_OK;
+}
+
+int check_device(const fir_os_plan *p) {
+    int dev = -1;
+    FOS_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != p->device)
+        return fail(FIR_OS_E_INVAL, "plan was created on device %d but device %d is current", p->device, dev);
+    return FIR_OS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fir_os_status_string(int status) {
+    switch (status) {
+        case FIR_OS_OK: return "ok";
+        case FIR_OS_E_INVAL: return "invalid argument";
+        case FIR_OS_E_UNSUPPORTED: return "unsupported configuration";
+        case FIR_OS_E_ALIGN: return "misaligned buffer";
+        case FIR_OS_E_NOMEM: return "out of memory";
+        case FIR_OS_E_CUDA: return "CUDA error";
+        case FIR_OS_E_DEVICE: return "device-side wait ran out";
+        default: return "unknown status";
+    }
+}
+
+const char *fir_os_last_error(void) { return g_last_error; }
+
+int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef_kind, int coef_complex,
+                       const void *coef_dev, void *stream_) {
+    g_last_error[0] = 0;
+    if (!out) return fail(FIR_OS_E_INVAL, "out is NULL");
+    *out = nullptr;
+    if (N < 64 || N > 65536 || (N & (N - 1)) != 0)
+        return fail(FIR_OS_E_UNSUPPORTED, "N = %d is not a power of two in [64, 65536]", N);
+    if (M < 1 || M > N) return fail(FIR_OS_E_UNSUPPORTED, "M = %d must be in [1, N = %d]", M, N);
+    if (data_kind != FIR_OS_REAL && data_kind != FIR_OS_COMPLEX)
+        return fail(FIR_OS_E_INVAL, "data_kind %d is neither FIR_OS_REAL nor FIR_OS_COMPLEX", data_kind);
+    if (coef_kind != FIR_OS_COEF_TIME && coef_kind != FIR_OS_COEF_FREQ)
+        return fail(FIR_OS_E_INVAL, "coef_kind %d is neither FIR_OS_COEF_TIME nor FIR_OS_COEF_FREQ", coef_kind);
+    if (coef_kind == FIR_OS_COEF_TIME && coef_complex != 0 && coef_complex != 1)
+        return fail(FIR_OS_E_INVAL, "coef_complex must be 0 or 1");
+    if (!coef_dev) return fail(FIR_OS_E_INVAL, "coef_dev is NULL");
+    if (coef_kind == FIR_OS_COEF_TIME && data_kind == FIR_OS_REAL && coef_complex)
+        return fail(FIR_OS_E_UNSUPPORTED, "real data needs a real h");
+    if (coef_kind == FIR_OS_COEF_FREQ && (reinterpret_cast<uintptr_t>(coef_dev) & 15))
+        return fail(FIR_OS_E_ALIGN, "a given H must be 16-byte aligned");
+    if (coef_kind == FIR_OS_COEF_TIME && (reinterpret_cast<uintptr_t>(coef_dev) & (coef_complex ? 7 : 3)))
+        return fail(FIR_OS_E_ALIGN, "h must be naturally aligned");
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    fir_os_plan *p = new (std::nothrow) fir_os_plan;
+    if (!p) return fail(FIR_OS_E_NOMEM, "plan allocation failed");
+    int rc = FIR_OS_OK;
+    auto bail = [&](int status) {
+        free_plan(p);
+        return status;
+    };
+    p->M = M;
+    p->N = N;
+    p->L = N - M + 1;
+    p->data_kind = data_kind;
+    {
+        cudaError_t e = cudaGetDevice(&p->device);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaGetDevice"));
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, p->device);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaGetDeviceProperties"));
+        if (!(prop.major == 10 && prop.minor == 3))
+            return bail(fail(FIR_OS_E_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                             p->device, prop.major, prop.minor));
+        p->sms = prop.multiProcessorCount;
+    }
+
+    const int logn = ilog2i(N);
+    const bool real = data_kind == FIR_OS_REAL;
+    if (logn <= 9) p->kernel = fos::block_kernel_small(logn, real);
+    else if (logn <= 13) p->kernel = fos::block_kernel_large(logn, real);
+    else p->kernel = fos::cluster_kernel(logn, real);
+    if (!p->kernel.func) return bail(fail(FIR_OS_E_UNSUPPORTED, "no kernel for N = %d", N));
+
+    // launch shape
+    {
+        cudaError_t e = cudaFuncSetAttribute(p->kernel.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             p->kernel.smem);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+        if (p->kernel.cluster == 1) {
+            int per_sm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->kernel.func, p->kernel.threads,
+                                                              (size_t)p->kernel.smem);
+            if (e != cudaSuccess) return bail(cuda_fail(e, "occupancy query"));
+            if (per_sm < 1) return bail(fail(FIR_OS_E_UNSUPPORTED, "block kernel does not fit an SM"));
+            p->max_units_in_flight = per_sm * p->sms;
+        } else {
+            if (p->kernel.cluster > 8) {
+                e = cudaFuncSetAttribute(p->kernel.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(cluster size)"));
+            }
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(p->kernel.cluster * 64);
+            cfg.blockDim = dim3(p->kernel.threads);
+            cfg.dynamicSmemBytes = (size_t)p->kernel.smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = p->kernel.cluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, p->kernel.func, &cfg);
+            if (e != cudaSuccess) return bail(cuda_fail(e, "cluster occupancy query"));
+            if (clusters < 1)
+                return bail(fail(FIR_OS_E_UNSUPPORTED, "a cluster of %d CTAs cannot be resident", p->kernel.cluster));
+            p->max_units_in_flight = clusters;
+        }
+    }
+
+    // device memory
+    {
+        cudaError_t e;
+        if ((e = cudaMalloc(&p->d_H, sizeof(float2) * N)) != cudaSuccess ||
+            (e = cudaMalloc(&p->d_err, sizeof(int))) != cudaSuccess)
+            return bail(e == cudaErrorMemoryAllocation ? fail(FIR_OS_E_NOMEM, "cudaMalloc failed")
+                                                       : cuda_fail(e, "cudaMalloc"));
+        std::vector<float2> tw;
+        if (!pass_twiddles(p->kernel.fft_logn, tw)) return bail(fail(FIR_OS_E_UNSUPPORTED, "twiddles"));
+        if ((e = cudaMalloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess)
+            return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(twiddles) failed"));
+        if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice,
+                                 stream)) != cudaSuccess)
+            return bail(cuda_fail(e, "twiddle upload"));
+        if (p->kernel.cluster > 1) {
+            const int P = 1 << p->kernel.fft_logn, C = N / P;
+            std::vector<float2> twa((size_t)N);
+            for (int c = 0; c < C; ++c)
+                for (int b = 0; b < P; ++b) {
+                    const long long ex = ((long long)b * c) % N;
+                    const double ang = -2.0 * M_PI * (double)ex / (double)N;
+                    twa[(size_t)c * P + b] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+                }
+            if ((e = cudaMalloc(&p->d_twa, sizeof(float2) * N)) != cudaSuccess)
+                return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(cluster twiddles) failed"));
+            if ((e = cudaMemcpyAsync(p->d_twa, twa.data(), sizeof(float2) * N, cudaMemcpyHostToDevice, stream)) !=
+                cudaSuccess)
+                return bail(cuda_fail(e, "cluster twiddle upload"));
+            // the host vectors must outlive the asynchronous copies
+            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
+        }
+        if ((e = cudaMemsetAsync(p->d_err, 0, sizeof(int), stream)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaMemsetAsync"));
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
+    }
+
+    // step 1: the frequency response
+    const int tpb = 256;
+    if (coef_kind == FIR_OS_COEF_TIME) {
+        double2 *A = nullptr, *B = nullptr;
+        cudaError_t e;
+        if ((e = cudaMalloc(&A, sizeof(double2) * N)) != cudaSuccess ||
+            (e = cudaMalloc(&B, sizeof(double2) * N)) != cudaSuccess) {
+            cudaFree(A);
+            return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(plan scratch) failed"));
+        }
+        fos_fill_h64<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, coef_dev, M, N, coef_complex);
+        for (int Ns = 1; Ns < N; Ns *= 2) {
+            fos_radix2_pass64<<<(N / 2 + tpb - 1) / tpb, tpb, 0, stream>>>(A, B, N, Ns);
+            double2 *t = A;
+            A = B;
+            B = t;
+        }
+        fos_finish_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, p->d_H, N);
+        e = cudaGetLastError();
+        cudaError_t e2 = cudaStreamSynchronize(stream);
+        cudaFree(A);
+        cudaFree(B);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "frequency-response kernels"));
+        if (e2 != cudaSuccess) return bail(cuda_fail(e2, "frequency-response sync"));
+    } else {
+        fos_scale_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(static_cast<const float2 *>(coef_dev), p->d_H, N);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return bail(cuda_fail(e, "H copy kernel"));
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "H copy sync"));
+        if (real) {
+            // real data packs two blocks per transform, which needs a real impulse response:
+            // H[k] == conj(H[N-k]) within 1e-6 of the largest bin
+            std::vector<float2> H((size_t)N);
+            if ((e = cudaMemcpy(H.data(), p->d_H, sizeof(float2) * N, cudaMemcpyDeviceToHost)) != cudaSuccess)
+                return bail(cuda_fail(e, "H readback"));
+            double hmax = 0.0, dev = 0.0;
+            for (int k = 0; k < N; ++k) hmax = std::fmax(hmax, std::hypot((double)H[k].x, (double)H[k].y));
+            for (int k = 0; k < N; ++k) {
+                const float2 a = H[k], b = H[(N - k) % N];
+                dev = std::fmax(dev, std::hypot((double)a.x - b.x, (double)a.y + b.y));
+            }
+            if (dev > 1e-6 * hmax)
+                return bail(fail(FIR_OS_E_UNSUPPORTED, "real data needs a Hermitian H (deviation %.3g of max %.3g)",
+                                 dev, hmax));
+        }
+    }
+    (void)rc;
+    *out = p;
+    return FIR_OS_OK;
+}
+
+int fir_os_plan_destroy(fir_os_plan_t plan) {
+    if (!plan) return FIR_OS_OK;
+    cudaDeviceSynchronize();
+    free_plan(plan);
+    return FIR_OS_OK;
+}
+
+int fir_os_plan_info(fir_os_plan_t plan, int *M, int *N, int *L) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (M) *M = plan->M;
+    if (N) *N = plan->N;
+    if (L) *L = plan->L;
+    return FIR_OS_OK;
+}
+
+int fir_os_plan_kernel(fir_os_plan_t plan, int *kind, int *cluster_size, int *grid, int *smem_bytes) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (kind) *kind = plan->kernel.cluster > 1 ? 1 : 0;
+    if (cluster_size) *cluster_size = plan->kernel.cluster;
+    if (grid) *grid = plan->max_units_in_flight * plan->kernel.cluster;
+    if (smem_bytes) *smem_bytes = plan->kernel.smem;
+    return FIR_OS_OK;
+}
+
+int fir_os_execute(fir_os_plan_t plan, const void *x, int64_t n, void *y, void *state, void *stream_) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (n < 0) return fail(FIR_OS_E_INVAL, "n_samples < 0");
+    if (n == 0) return FIR_OS_OK;
+    const int sb = sample_bytes(plan);
+    if (!x || !y) return fail(FIR_OS_E_INVAL, "x or y is NULL");
+    if (plan->M > 1 && !state) return fail(FIR_OS_E_INVAL, "state is NULL but M > 1");
+    const uintptr_t ux = reinterpret_cast<uintptr_t>(x), uy = reinterpret_cast<uintptr_t>(y),
+                    us = reinterpret_cast<uintptr_t>(state);
+    if ((ux | uy) & (uintptr_t)(sb - 1) || (plan->M > 1 && (us & (uintptr_t)(sb - 1))))
+        return fail(FIR_OS_E_ALIGN, "x, y and state must be %d-byte aligned", sb);
+    const size_t bytes = (size_t)n * sb, sbytes = (size_t)(plan->M - 1) * sb;
+    if (ranges_overlap(ux, bytes, uy, bytes)) return fail(FIR_OS_E_INVAL, "x and y overlap");
+    if (ranges_overlap(us, sbytes, ux, bytes) || ranges_overlap(us, sbytes, uy, bytes))
+        return fail(FIR_OS_E_INVAL, "state overlaps x or y");
+    int rc = check_device(plan);
+    if (rc) return rc;
+    return launch_blocks(plan, x, n, y, state, static_cast<cudaStream_t>(stream_));
+}
+
+int fir_os_launches(fir_os_plan_t plan, int64_t n) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (n < 0) return fail(FIR_OS_E_INVAL, "n_samples < 0");
+    if (n == 0) return 0;
+    return fuse_state(plan, n) ? 1 : 2;
+}
+
+int fir_os_device_status(fir_os_plan_t plan, void *stream_) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    int rc = check_device(plan);
+    if (rc) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int flag = 0;
+    FOS_CUDA(cudaMemcpyAsync(&flag, plan->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream), "status read");
+    FOS_CUDA(cudaMemsetAsync(plan->d_err, 0, sizeof(int), stream), "status clear");
+    FOS_CUDA(cudaStreamSynchronize(stream), "status sync");
+    if (flag) return fail(FIR_OS_E_DEVICE, "a kernel's bounded wait for a bulk copy ran out");
+    return FIR_OS_OK;
+}
+
+int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n, void *y_host, void *state_host,
+                        void *stream_) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (n < 0) return fail(FIR_OS_E_INVAL, "n_samples < 0");
+    if (plan->M > 1 && !state_host) return fail(FIR_OS_E_INVAL, "state is NULL but M > 1");
+    if (n > 0 && (!x_host || !y_host)) return fail(FIR_OS_E_INVAL, "x or y is NULL");
+    int rc = check_device(plan);
+    if (rc) return rc;
+    const int sb = sample_bytes(plan);
+    const size_t sbytes = (size_t)(plan->M - 1) * sb;
+    if (n > 0 && ranges_overlap(reinterpret_cast<uintptr_t>(x_host), (size_t)n * sb,
+                                reinterpret_cast<uintptr_t>(y_host), (size_t)n * sb))
+        return fail(FIR_OS_E_INVAL, "x and y overlap");
+    cudaStream_t caller = static_cast<cudaStream_t>(stream_);
+
+    if (!plan->s_comp) {
+        // chunks of about 2^21 samples, a whole number of blocks, so a chunked call cuts the
+        // stream at the same block boundaries as one device call
+        int64_t chunk = ((int64_t)1 << 21) / plan->L * plan->L;
+        if (chunk < plan->L) chunk = plan->L;
+        plan->host_chunk = chunk;
+        for (int k = 0; k < 2; ++k) {
+            cudaError_t e1 = cudaMalloc(&plan->hx[k], (size_t)chunk * sb);
+            cudaError_t e2 = cudaMalloc(&plan->hy[k], (size_t)chunk * sb);
+            if (e1 != cudaSuccess || e2 != cudaSuccess) return fail(FIR_OS_E_NOMEM, "cudaMalloc(host path buffers)");
+            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_in[k], cudaEventDisableTiming), "event");
+            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_comp[k], cudaEventDisableTiming), "event");
+            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_out[k], cudaEventDisableTiming), "event");
+        }
+        if (plan->M > 1 && cudaMalloc(&plan->hstate, sbytes) != cudaSuccess)
+            return fail(FIR_OS_E_NOMEM, "cudaMalloc(host path state)");
+        FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_start, cudaEventDisableTiming), "event");
+        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking), "stream");
+        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking), "stream");
+        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_comp, cudaStreamNonBlocking), "stream");
+    }
+    const int64_t chunk = plan->host_chunk;
+    FOS_CUDA(cudaEventRecord(plan->ev_start, caller), "event record");
+    FOS_CUDA(cudaStreamWaitEvent(plan->s_in, plan->ev_start, 0), "wait");
+    FOS_CUDA(cudaStreamWaitEvent(plan->s_comp, plan->ev_start, 0), "wait");
+    FOS_CUDA(cudaStreamWaitEvent(plan->s_out, plan->ev_start, 0), "wait");
+    if (plan->M > 1)
+        FOS_CUDA(cudaMemcpyAsync(plan->hstate, state_host, sbytes, cudaMemcpyHostToDevice, plan->s_comp), "state in");
+    const char *xs = static_cast<const char *>(x_host);
+    char *ys = static_cast<char *>(y_host);
+    int64_t c = 0;
+    for (int64_t off = 0; off < n; off += chunk, ++c) {
+        const int k = (int)(c & 1);
+        const int64_t len = (n - off) < chunk ? (n - off) : chunk;
+        if (c >= 2) FOS_CUDA(cudaStreamWaitEvent(plan->s_in, plan->ev_comp[k], 0), "wait");
+        FOS_CUDA(cudaMemcpyAsync(plan->hx[k], xs + off * sb, (size_t)len * sb, cudaMemcpyHostToDevice, plan->s_in),
+                 "chunk in");
+        FOS_CUDA(cudaEventRecord(plan->ev_in[k], plan->s_in), "event record");
+        FOS_CUDA(cudaStreamWaitEvent(plan->s_comp, plan->ev_in[k], 0), "wait");
+        if (c >= 2) FOS_CUDA(cudaStreamWaitEvent(plan->s_comp, plan->ev_out[k], 0), "wait");
+        rc = launch_blocks(plan, plan->hx[k], len, plan->hy[k], plan->hstate, plan->s_comp);
+        if (rc) return rc;
+        FOS_CUDA(cudaEventRecord(plan->ev_comp[k], plan->s_comp), "event record");
+        FOS_CUDA(cudaStreamWaitEvent(plan->s_out, plan->ev_comp[k], 0), "wait");
+        FOS_CUDA(cudaMemcpyAsync(ys + off * sb, plan->hy[k], (size_t)len * sb, cudaMemcpyDeviceToHost, plan->s_out),
+                 "chunk out");
+        FOS_CUDA(cudaEventRecord(plan->ev_out[k], plan->s_out), "event record");
+    }
+    if (plan->M > 1)
+        FOS_CUDA(cudaMemcpyAsync(state_host, plan->hstate, sbytes, cudaMemcpyDeviceToHost, plan->s_comp), "state out");
+    FOS_CUDA(cudaStreamSynchronize(plan->s_in), "sync");
+    FOS_CUDA(cudaStreamSynchronize(plan->s_comp), "sync");
+    FOS_CUDA(cudaStreamSynchronize(plan->s_out), "sync");
+    return FIR_OS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,267 @@
+// fos_device.cuh -- device building blocks for the overlap-save block kernels (sm_103a).
+//
+// Complex float32 arithmetic, small in-register DFTs (radix 2, 4, 8, 16), the shared-memory
+// swizzle used by the Stockham exchange passes, and thin inline-PTX wrappers for mbarrier,
+// bulk (TMA) copies, cluster barriers and distributed shared memory.
+//
+// The transform convention follows the reading of "一种基于GPU的高阶数字FIR滤波器频域并行处理
+// 实现方法" (zl.czvv.com/42398539.html) 主权项 step 4 used throughout this library: forward
+// e^{-2 pi i nk/N}, inverse e^{+2 pi i nk/N}; DIR = -1 selects the forward sign, +1 the
+// inverse (its 1/N is folded into the stored response H).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+// Pure arithmetic helpers are usable from host code too (host-side checks of the DFTs).
+#define FOS_HD __host__ __device__ __forceinline__
+
+namespace fos {
+
+// --------------------------------------------------------------------------- complex ops
+
+FOS_HD float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+FOS_HD float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+FOS_HD float2 cneg(float2 a) { return make_float2(-a.x, -a.y); }
+
+// a * w
+FOS_HD float2 cmul(float2 a, float2 w) {
+    return make_float2(fmaf(a.x, w.x, -a.y * w.y), fmaf(a.x, w.y, a.y * w.x));
+}
+// a * conj(w)
+FOS_HD float2 cmulc(float2 a, float2 w) {
+    return make_float2(fmaf(a.x, w.x, a.y * w.y), fmaf(a.y, w.x, -a.x * w.y));
+}
+// a * w for DIR = -1, a * conj(w) for DIR = +1 (w holds a forward-sign twiddle)
+template <int DIR>
+FOS_HD float2 ctw(float2 a, float2 w) {
+    if constexpr (DIR < 0) return cmul(a, w);
+    else return cmulc(a, w);
+}
+// a * (DIR * i): a rotation by a quarter turn in the transform's direction
+template <int DIR>
+FOS_HD float2 crot(float2 a) {
+    if constexpr (DIR < 0) return make_float2(a.y, -a.x);  // * (-i)
+    else return make_float2(-a.y, a.x);                    // * (+i)
+}
+
+// --------------------------------------------------------------------------- constant twiddles
+
+// cos and sin of 2 pi m / 16, m = 0..15 (exact decimal expansions of cos(pi/8), sin(pi/8),
+// sqrt(1/2), rounded by the compiler to float32).
+__host__ __device__ constexpr float cos16(int m) {
+    constexpr float c1 = 0.92387953251128675613f, s1 = 0.38268343236508977173f,
+                    h = 0.70710678118654752440f;
+    constexpr float t[16] = {1.f, c1, h, s1, 0.f, -s1, -h, -c1, -1.f, -c1, -h, -s1, 0.f, s1, h, c1};
+    return t[m & 15];
+}
+__host__ __device__ constexpr float sin16(int m) { return cos16(m - 4); }
+
+// a * e^{DIR * 2 pi i * m / R} for compile-time R (a power of two <= 16) and m,
+// with the trivial angles done by swaps and sign changes.
+template <int R, int M, int DIR>
+FOS_HD float2 ctw_const(float2 a) {
+    constexpr int m16 = ((M * (16 / R)) % 16 + 16) % 16;
+    if constexpr (m16 == 0) return a;
+    else if constexpr (m16 == 8) return cneg(a);
+    else if constexpr (m16 == 4) return crot<DIR>(a);
+    else if constexpr (m16 == 12) return crot<-DIR>(a);
+    else if constexpr (m16 % 2 == 0) {
+        // (+-1 +- i) / sqrt 2
+        constexpr float h = 0.70710678118654752440f;
+        constexpr float c = cos16(m16), s = (DIR < 0 ? -1.f : 1.f) * sin16(m16);
+        // c, s are each +-h
+        if constexpr (c > 0 && s > 0) return make_float2((a.x - a.y) * h, (a.x + a.y) * h);
+        else if constexpr (c > 0 && s < 0) return make_float2((a.x + a.y) * h, (a.y - a.x) * h);
+        else if constexpr (c < 0 && s > 0) return make_float2(-(a.x + a.y) * h, (a.x - a.y) * h);
+        else return make_float2((a.y - a.x) * h, -(a.x + a.y) * h);
+    } else {
+        constexpr float c = cos16(m16), s = (DIR < 0 ? -1.f : 1.f) * sin16(m16);
+        return cmul(a, make_float2(c, s));
+    }
+}
+
+// a * e^{DIR 2 pi i m / R} for an m that is a compile-time constant after unrolling.
+template <int R, int DIR>
+FOS_HD float2 ctw_dyn(float2 a, int m) {
+    switch (((m * (16 / R)) % 16 + 16) % 16) {
+        case 0: return a;
+        case 1: return ctw_const<16, 1, DIR>(a);
+        case 2: return ctw_const<16, 2, DIR>(a);
+        case 3: return ctw_const<16, 3, DIR>(a);
+        case 4: return ctw_const<16, 4, DIR>(a);
+        case 5: return ctw_const<16, 5, DIR>(a);
+        case 6: return ctw_const<16, 6, DIR>(a);
+        case 7: return ctw_const<16, 7, DIR>(a);
+        case 8: return ctw_const<16, 8, DIR>(a);
+        case 9: return ctw_const<16, 9, DIR>(a);
+        case 10: return ctw_const<16, 10, DIR>(a);
+        case 11: return ctw_const<16, 11, DIR>(a);
+        case 12: return ctw_const<16, 12, DIR>(a);
+        case 13: return ctw_const<16, 13, DIR>(a);
+        case 14: return ctw_const<16, 14, DIR>(a);
+        default: return ctw_const<16, 15, DIR>(a);
+    }
+}
+
+// --------------------------------------------------------------------------- small DFTs
+// In place, natural order in and out: a[k] <- sum_n a[n] e^{DIR 2 pi i nk/R}.
+
+template <int DIR>
+FOS_HD void dft2(float2 &a0, float2 &a1) {
+    float2 t = a0;
+    a0 = cadd(t, a1);
+    a1 = csub(t, a1);
+}
+
+template <int DIR>
+FOS_HD void dft4(float2 &a0, float2 &a1, float2 &a2, float2 &a3) {
+    float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), t3 = crot<DIR>(csub(a1, a3));
+    a0 = cadd(t0, t2);
+    a2 = csub(t0, t2);
+    a1 = cadd(t1, t3);
+    a3 = csub(t1, t3);
+}
+
+// R = R1 * 4 with n = 4 a + b, k = c + R1 d:
+//   X[c + R1 d] = sum_b W4^{bd} W_R^{bc} sum_a x[4a + b] W_R1^{ac}
+template <int R, int DIR>
+FOS_HD void dft(float2 *a) {
+    if constexpr (R == 1) {
+    } else if constexpr (R == 2) {
+        dft2<DIR>(a[0], a[1]);
+    } else if constexpr (R == 4) {
+        dft4<DIR>(a[0], a[1], a[2], a[3]);
+    } else {
+        constexpr int R1 = R / 4;
+        float2 y[4][R1];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+            for (int q = 0; q < R1; ++q) y[b][q] = a[4 * q + b];
+            dft<R1, DIR>(y[b]);
+        }
+        // twiddles W_R^{bc}
+#pragma unroll
+        for (int c = 1; c < R1; ++c) {
+            y[1][c] = ctw_dyn<R, DIR>(y[1][c], c);
+            y[2][c] = ctw_dyn<R, DIR>(y[2][c], 2 * c);
+            y[3][c] = ctw_dyn<R, DIR>(y[3][c], 3 * c);
+        }
+#pragma unroll
+        for (int c = 0; c < R1; ++c) {
+            dft4<DIR>(y[0][c], y[1][c], y[2][c], y[3][c]);
+#pragma unroll
+            for (int d = 0; d < 4; ++d) a[c + R1 * d] = y[d][c];
+        }
+    }
+}
+
+// --------------------------------------------------------------------------- exchange layout
+// Shared-memory index of logical element A of an exchange buffer: one padding element after
+// every 16, so a buffer of N elements occupies N + N/16.  With 8-byte elements this makes the
+// Stockham writes (stride Ns, or R0 for the first pass) and the reads (stride N/16) free of
+// bank conflicts, and keeps every per-thread address an affine function of the element index
+// (base + compile-time offset) whenever N/16 is a multiple of 16.
+FOS_HD int xpad(int A) { return A + (A >> 4); }
+__host__ __device__ constexpr int xpad_len(int n) { return n + n / 16; }
+
+// --------------------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Longest a kernel waits for one bulk copy before it reports FIR_OS_E_DEVICE (1 s).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Bounded wait for the phase with the given parity to complete; false if it ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// Bulk copy global -> this CTA's shared memory, completing `bytes` on the mbarrier.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// streaming (evict-first) global stores
+__device__ __forceinline__ void st_cs(float2 *p, float2 v) { __stcs(p, v); }
+__device__ __forceinline__ void st_cs(float *p, float v) { __stcs(p, v); }
+
+// --------------------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster; release/acquire orders shared-memory writes
+// (local and distributed) made before it with reads made after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+}  // namespace fos

@@ -1,0 +1,43 @@
+// fos_kernels.h -- host-side view of the block kernels (internal to libfir_os.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fos {
+
+// Arguments of one block-kernel launch (passed by value).
+struct BlockParams {
+    const void *x;         // n input samples (float or float2)
+    void *y;               // n output samples
+    void *state;           // M-1 samples of S0 in, S0' out (NULL when M == 1)
+    const float2 *H;       // N bins, H / N, natural order
+    const float2 *tw;      // Stockham pass twiddles of the per-CTA transform
+    const float2 *twa;     // cluster kernel: W_N^{b c} at [c * P + b]
+    int *err;              // device error word (set to 1 when a bounded wait ran out)
+    int64_t n;             // samples in this call
+    int64_t nunits;        // work units (block groups / blocks / block pairs)
+    int M;                 // taps
+    int L;                 // block length N - M + 1
+    int fuse_state;        // the kernel writes S0' itself (else a state kernel follows)
+};
+
+struct KernelEntry {
+    const void *func = nullptr;  // __global__ function
+    int threads = 0;             // threads per CTA
+    int smem = 0;                // dynamic shared memory per CTA (bytes)
+    int cluster = 1;             // CTAs per cluster (1 = no cluster)
+    int units_per_cta = 1;       // blocks (complex) or block pairs (real) per work unit
+    int fft_logn = 0;            // log2 of the per-CTA transform size (twiddle table shape)
+};
+
+// Single-CTA kernels, N = 2^logn, logn in [6, 13].
+KernelEntry block_kernel_small(int logn, bool real);   // logn 6..9
+KernelEntry block_kernel_large(int logn, bool real);   // logn 10..13
+// Cluster kernels, N = 2^logn, logn in [14, 16].
+KernelEntry cluster_kernel(int logn, bool real);
+
+// Entries of the pass-twiddle table for a per-CTA transform of 2^logn points.
+int pass_twiddle_entries(int logn);
+
+}  // namespace fos

@@ -1,0 +1,163 @@
+/*
+ * fir_os.h -- C ABI of libfir_os.so: high-order FIR filtering by the frequency-domain
+ * overlap-save method on one GB300 (sm_103a).
+ *
+ * The method is the one claimed in "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法"
+ * (zl.czvv.com/42398539.html), 主权项 steps 1-6:
+ *   step 1  an M-tap impulse response h is zero-padded to N and transformed, H = FFT_N(h),
+ *           or the N-point response H is given directly;
+ *   step 2  the input is cut into blocks B_i of L = N - M + 1 samples;
+ *   step 3  each block is extended by the M-1 samples before it, E_0 = {S0, B_0},
+ *           E_i = {D_{i-1}, B_i}, and the newest M-1 samples are carried as the next S0;
+ *   step 4  R_i = IFFT(FFT(E_i) * H);
+ *   step 5  the first M-1 samples of each R_i are dropped, Y_i = R_i[M-1 .. M-1+L);
+ *   step 6  the caller repeats with the next chunk of input.
+ * Together these compute, for every output j of a call,
+ *       y[j] = sum_{m=0}^{M-1} h[m] * xt[j-m],   xt[t] = x[t] (t >= 0), S0[M-1+t] (t < 0),
+ * a linear convolution continued seamlessly across calls.
+ *
+ * Conventions: the forward transform is e^{-2 pi i nk/N} unscaled and the inverse is
+ * e^{+2 pi i nk/N} scaled by 1/N; a given H is therefore the unscaled FFT of the taps.
+ * Samples are float32 (real data) or interleaved float32 (re, im) pairs (complex64).
+ * All arithmetic on the device is float32.
+ *
+ * Errors: every entry point returns FIR_OS_OK (0) or a negative status; no call throws,
+ * traps on the device or aborts.  Arguments are validated on the host before anything is
+ * enqueued.  fir_os_last_error() gives a one-line description of the last failure on the
+ * calling thread.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ * Device work is enqueued asynchronously on it unless stated otherwise.
+ */
+#ifndef FIR_OS_H
+#define FIR_OS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define FIR_OS_OK 0
+#define FIR_OS_E_INVAL (-1)       /* null pointer, bad size, overlapping buffers, bad kind */
+#define FIR_OS_E_UNSUPPORTED (-2) /* N not a power of two in [64, 65536], M > N, real data
+                                     with a complex or non-Hermitian response, no device */
+#define FIR_OS_E_ALIGN (-3)       /* a buffer without the alignment stated below */
+#define FIR_OS_E_NOMEM (-4)       /* device or host allocation failed */
+#define FIR_OS_E_CUDA (-5)        /* a CUDA runtime call or a launch failed */
+#define FIR_OS_E_DEVICE (-6)      /* a kernel reported a bounded wait that ran out */
+
+/* data kinds */
+#define FIR_OS_REAL 0    /* x, y, state: float32 */
+#define FIR_OS_COMPLEX 1 /* x, y, state: complex64 (float32 re, im interleaved) */
+
+/* coefficient kinds */
+#define FIR_OS_COEF_TIME 0 /* coef = h, M taps (step 1, first case) */
+#define FIR_OS_COEF_FREQ 1 /* coef = H, N bins of complex64 (step 1, second case) */
+
+typedef struct fir_os_plan *fir_os_plan_t;
+
+/*
+ * fir_os_plan_create -- step 1: build the frequency response and everything the block
+ * kernels need for one (M, N, data kind) combination.
+ *
+ *   out          receives the plan handle (set to NULL on failure)
+ *   M            taps, 1 <= M <= N
+ *   N            FFT size, a power of two in [64, 65536]; the block length is L = N - M + 1
+ *   data_kind    FIR_OS_REAL or FIR_OS_COMPLEX (the x / y / state sample type)
+ *   coef_kind    FIR_OS_COEF_TIME: coef_dev holds h[0..M-1]; H = FFT_N(h zero-padded to N)
+ *                is computed on the device in float64 and rounded to complex64.
+ *                FIR_OS_COEF_FREQ: coef_dev holds H[0..N-1] (complex64) and must be
+ *                16-byte aligned (the claim stores H at an address that is a multiple of
+ *                the memory width); it is copied.
+ *   coef_complex for COEF_TIME: 0 = h is float32, 1 = h is complex64.  Ignored for FREQ.
+ *                Real data needs a real h, or (FREQ) an H that is Hermitian within 1e-6 of
+ *                its largest bin; otherwise FIR_OS_E_UNSUPPORTED.
+ *   coef_dev     device pointer, owned by the caller; it may be freed once this returns
+ *   stream       the plan-time kernels run on it; the call synchronises it before returning
+ *
+ * The plan owns its device memory (H scaled by 1/N, twiddle tables, an error word) and
+ * keeps the device that was current at creation; later calls must be made with that
+ * device current.
+ */
+int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef_kind,
+                       int coef_complex, const void *coef_dev, void *stream);
+
+/*
+ * fir_os_execute -- steps 2-5 for one chunk of n_samples input samples, asynchronously on
+ * `stream`.
+ *
+ *   x_dev      n_samples input samples (device), naturally aligned (4 B real, 8 B complex)
+ *   n_samples  >= 0; 0 is a no-op.  Need not be a multiple of L: the last block is
+ *              zero-padded past the input and only n_samples outputs are written.
+ *   y_dev      n_samples output samples (device), same type and alignment as x; must not
+ *              overlap x or the state
+ *   state_dev  M-1 samples (device, oldest first) holding S0 on entry and, in stream order
+ *              after the call, the newest M-1 samples of concat(S0, x): the next call's S0.
+ *              Zero it before the first call of a stream.  May be NULL only when M == 1.
+ *
+ * Returns after enqueueing; y and the state are valid in stream order.  Concurrent calls
+ * that share a state buffer must be serialised by the caller.  A device-side wait that
+ * ran out is reported later by fir_os_device_status().
+ */
+int fir_os_execute(fir_os_plan_t plan, const void *x_dev, int64_t n_samples, void *y_dev,
+                   void *state_dev, void *stream);
+
+/*
+ * fir_os_execute_host -- the same filtering for input and output in HOST memory: step 2
+ * and step 6 of the claim (copy a chunk in, filter it, copy the result out, repeat while
+ * data remains), pipelined over two device buffer sets so that the copies of one chunk
+ * overlap the filtering of the next.  Synchronous: returns when y_host and state_host
+ * hold the results.
+ *
+ *   x_host, y_host   n_samples samples each, host memory (page-locked memory gives
+ *                    asynchronous copies; pageable memory works but serialises them)
+ *   state_host       M-1 samples in/out (host), as for fir_os_execute; NULL only if M == 1
+ *   stream           the caller's stream; work is ordered after it and it is synchronised
+ *
+ * The plan allocates its device buffers for this call on first use (two input and two
+ * output chunks of about 2^21 samples, a whole number of blocks, so the chunks cut the stream
+ * at the same block boundaries as one fir_os_execute call) and keeps them until
+ * fir_os_plan_destroy.
+ */
+int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n_samples,
+                        void *y_host, void *state_host, void *stream);
+
+/* fir_os_plan_destroy -- synchronises the device work of the plan and frees it. NULL is a
+ * no-op. */
+int fir_os_plan_destroy(fir_os_plan_t plan);
+
+/* fir_os_plan_info -- M, N and L = N - M + 1 of a plan (any output pointer may be NULL). */
+int fir_os_plan_info(fir_os_plan_t plan, int *M, int *N, int *L);
+
+/* fir_os_plan_kernel -- which block kernel a plan launches: 0 = one CTA per block group
+ * (N <= 8192), 1 = a thread-block cluster per block (N >= 16384).  *cluster_size is 1 or
+ * the cluster's CTA count; *grid the CTAs one launch uses; *smem_bytes the dynamic shared
+ * memory per CTA.  Any output pointer may be NULL. */
+int fir_os_plan_kernel(fir_os_plan_t plan, int *kind, int *cluster_size, int *grid,
+                       int *smem_bytes);
+
+/* fir_os_launches -- how many kernels one fir_os_execute call of n_samples launches: 0 for
+ * n_samples == 0, else 1 (the fused block kernel, which also writes the new state) or 2 (the
+ * block kernel and a one-CTA state kernel, when more than one work unit reads S0).
+ * Returns a negative status for a bad plan or n_samples < 0. */
+int fir_os_launches(fir_os_plan_t plan, int64_t n_samples);
+
+/* fir_os_device_status -- synchronises `stream`, then reads and clears the plan's device
+ * error word: FIR_OS_OK, or FIR_OS_E_DEVICE if a kernel's bounded wait ran out since the
+ * last check. */
+int fir_os_device_status(fir_os_plan_t plan, void *stream);
+
+/* fir_os_status_string -- a static description of a status code. */
+const char *fir_os_status_string(int status);
+
+/* fir_os_last_error -- the calling thread's description of its last failed call (static
+ * storage, overwritten by the next failure; "" if none). */
+const char *fir_os_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FIR_OS_H */
