@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -109,6 +110,40 @@ __global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist) {
         if (t < hist) state[t] = v;
         __syncthreads();
     }
+}
+
+// ------------------------------------------------------------------ allocation-free response
+// fir_os_frequency_response_noalloc runs the float64 step-1 transform above with its two
+// ping-pong buffers taken from this fixed device array instead of cudaMalloc.  Every device
+// that loads the library holds these 2 MiB until the process exits; all calls share them.
+constexpr int kNoallocMaxN = 65536;
+static __device__ __align__(256) double2 g_noalloc_scratch[2 * kNoallocMaxN];
+
+// H[t] = A[t] rounded to complex64 (unscaled, as a given response is passed to a plan).
+__global__ void fos_store_h(const double2 *A, float2 *H, int N) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < N) H[t] = make_float2((float)A[t].x, (float)A[t].y);
+}
+
+std::mutex g_noalloc_mu;
+double2 *g_noalloc_ptr[128] = {};
+
+// Device address of the scratch array for the current device, looked up once per device
+// with that device current (the array's name is only a host-side stand-in in host code).
+int noalloc_scratch(double2 **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 128) return fail(FIR_OS_E_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_ptr[dev] = static_cast<double2 *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FIR_OS_OK;
 }
 
 // ------------------------------------------------------------------ plan
@@ -604,6 +639,37 @@ int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n, void 
     FOS_CUDA(cudaStreamSynchronize(plan->s_in), "sync");
     FOS_CUDA(cudaStreamSynchronize(plan->s_comp), "sync");
     FOS_CUDA(cudaStreamSynchronize(plan->s_out), "sync");
+    return FIR_OS_OK;
+}
+
+int fir_os_frequency_response_noalloc(const void *h_dev, int M, int N, int h_complex, void *H_dev,
+                                      void *stream_) {
+    if (!h_dev || !H_dev) return fail(FIR_OS_E_INVAL, "h or H is NULL");
+    if (N > kNoallocMaxN)
+        return fail(FIR_OS_E_UNSUPPORTED, "N = %d exceeds the %d points the static scratch holds", N, kNoallocMaxN);
+    if (N < 64 || (N & (N - 1)) != 0)
+        return fail(FIR_OS_E_UNSUPPORTED, "N = %d is not a power of two in [64, %d]", N, kNoallocMaxN);
+    if (M < 1 || M > N) return fail(FIR_OS_E_UNSUPPORTED, "M = %d must be in [1, N = %d]", M, N);
+    if (h_complex != 0 && h_complex != 1) return fail(FIR_OS_E_INVAL, "h_complex must be 0 or 1");
+    if (reinterpret_cast<uintptr_t>(h_dev) & (h_complex ? 7 : 3))
+        return fail(FIR_OS_E_ALIGN, "h must be naturally aligned");
+    if (reinterpret_cast<uintptr_t>(H_dev) & 7) return fail(FIR_OS_E_ALIGN, "H must be 8-byte aligned");
+    double2 *scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    double2 *A = scratch, *B = scratch + kNoallocMaxN;
+    const int tpb = 256;
+    // every entry of A[0..N) is written here, so nothing left by an earlier call is read
+    fos_fill_h64<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, h_dev, M, N, h_complex);
+    for (int Ns = 1; Ns < N; Ns *= 2) {
+        fos_radix2_pass64<<<(N / 2 + tpb - 1) / tpb, tpb, 0, stream>>>(A, B, N, Ns);
+        double2 *t = A;
+        A = B;
+        B = t;
+    }
+    fos_store_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, static_cast<float2 *>(H_dev), N);
+    FOS_CUDA(cudaGetLastError(), "frequency-response kernels");
     return FIR_OS_OK;
 }
 

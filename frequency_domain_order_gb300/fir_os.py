@@ -41,6 +41,7 @@ SIGNATURES = {
                                 ctypes.POINTER(_I)]),
     "fir_os_device_status": (_I, [_P, _P]),
     "fir_os_launches": (_I, [_P, _I64]),
+    "fir_os_frequency_response_noalloc": (_I, [_P, _I, _I, _I, _P, _P]),
     "fir_os_status_string": (ctypes.c_char_p, [_I]),
     "fir_os_last_error": (ctypes.c_char_p, []),
 }

@@ -149,6 +149,35 @@ int fir_os_launches(fir_os_plan_t plan, int64_t n_samples);
  * last check. */
 int fir_os_device_status(fir_os_plan_t plan, void *stream);
 
+/*
+ * fir_os_frequency_response_noalloc -- H = FFT_N(h zero-padded to N), the unscaled
+ * complex64 response that fir_os_plan_create accepts as FIR_OS_COEF_FREQ, computed on the
+ * device in float64 without allocating any memory.  The paper has no counterpart of this
+ * entry point; it exists for callers that must not allocate device memory at the point where
+ * they build a response: code whose device memory is handed out entirely by its own pool,
+ * real-time threads that cannot afford an allocation's unbounded latency, or a process that
+ * is at its memory limit.  fir_os_plan_create needs float64 working buffers for the same
+ * transform and allocates them; this call uses a fixed 2 MiB array in the library's device
+ * image instead (held by every device that loads the library until the process exits).
+ *
+ *   h_dev      M taps (device): float32 if h_complex == 0, complex64 if 1, naturally aligned
+ *   M          1 <= M <= N
+ *   N          a power of two in [64, 65536]; larger N is rejected (FIR_OS_E_UNSUPPORTED)
+ *              because the fixed array holds two 65536-point float64 buffers and no more
+ *   H_dev      N complex64 bins (device, 8-byte aligned; 16-byte aligned if it is to be
+ *              passed to fir_os_plan_create), written in stream order
+ *   stream     the kernels are enqueued on it asynchronously
+ *
+ * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call on a device
+ * looks up the device address of the fixed array (once per device, with that device
+ * current); make that first call before any stream capture.  All calls share the one array
+ * and leave their intermediate values in it; each call rewrites every entry it reads, but
+ * calls whose kernels overlap on the GPU (different streams, or different host threads
+ * without ordering) race on the array and must be serialised by the caller.
+ */
+int fir_os_frequency_response_noalloc(const void *h_dev, int M, int N, int h_complex,
+                                      void *H_dev, void *stream);
+
 /* fir_os_status_string -- a static description of a status code. */
 const char *fir_os_status_string(int status);
 
