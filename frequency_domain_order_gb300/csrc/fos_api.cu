@@ -270,7 +270,9 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.M = p->M;
     bp.L = p->L;
     bp.fuse_state = fuse_state(p, n);
-    const int64_t groups = bp.nunits < p->max_units_in_flight ? bp.nunits : p->max_units_in_flight;
+    // CTAs (or clusters) to launch: enough groups for every unit, at most what is resident
+    const int64_t want = (bp.nunits + p->kernel.groups - 1) / p->kernel.groups;
+    const int64_t groups = want < p->max_units_in_flight ? want : p->max_units_in_flight;
     void *args[] = {&bp};
     if (p->kernel.cluster == 1) {
         FOS_CUDA(cudaLaunchKernel(p->kernel.func, dim3((unsigned)groups), dim3(p->kernel.threads), args,

@@ -7,9 +7,9 @@
 //            groups of blocks arrive by one bulk (TMA) copy issued while the previous group
 //            is being transformed (double-buffered); groups that touch the state S0 or run
 //            past the input are gathered with plain loads (S0 in front, zeros behind).
-//   FFT      F_i = FFT_N(E_i) in registers + the exchange buffer (fos_fft.cuh)
-//   multiply I_i = F_i * H with H / N held in shared memory for the life of the CTA
-//   IFFT     R_i = IFFT_N(I_i), again natural order in registers
+//   FFT      F_i = FFT_N(E_i) in registers and two alternating exchange buffers
+//   multiply I_i = F_i * H
+//   IFFT     R_i = IFFT_N(I_i), natural order in registers
 //   discard  Y_i = R_i[M-1 .. M-1+L) stored straight from registers, masked to n outputs
 //   state    the CTA holding block 0 writes S0' = last M-1 samples of concat(S0, x)
 //            after it has read S0 (no other CTA reads S0 when fuse_state is set)
@@ -17,9 +17,19 @@
 // E_{2p+1} as imaginary part); with a real h the two outputs come back as the real and
 // imaginary parts of R.
 //
-// Grid: persistent, at most (SMs x resident CTAs) CTAs; CTA c takes work units c, c + grid,
-// ...  A work unit is F consecutive blocks (complex) or F consecutive block pairs (real),
-// F = max(1, 256 / (N/16)), each handled by N/16 threads.
+// Per-thread constants -- the 16 bins of H / N a thread multiplies and the twiddles of its
+// passes -- are written once into Tensor Memory (this thread's lane) and read back with
+// tcgen05.ld for every block, keeping them off the shared-memory / L1 path that carries the
+// exchanges.  Each group's shared memory holds three buffers: two staging windows (the one being filtered
+// and the one being fetched) and one exchange buffer; the window being filtered doubles as
+// the second exchange buffer once it has been read.
+//
+// A CTA that allocates Tensor Memory runs alone on its SM, so a CTA has 512 threads split
+// into independent groups (two groups of 256 for N <= 4096, one of 512 for N = 8192), each
+// with its own three buffers, mbarriers and hardware barrier, sharing only the Tensor Memory
+// allocation.  Grid: persistent, one CTA per SM; the groups of all CTAs take work units
+// round-robin.  A work unit is F consecutive blocks (complex) or F consecutive block pairs
+// (real), F = max(1, 256 / (N/16)), each handled by N/16 threads.
 #pragma once
 
 #include <type_traits>
@@ -35,16 +45,27 @@ struct BlockCfg {
     static constexpr int N = S::N;
     static constexpr int T = S::T;
     static constexpr int F = T >= 256 ? 1 : 256 / T;
-    static constexpr int THREADS = F * T;
+    static constexpr int GT = F * T;              // threads of one group (256, or 512 for N = 8192)
+    static constexpr int GROUPS = 512 / GT;       // independent groups per CTA
+    static constexpr int THREADS = 512;
     static constexpr int SB = REAL ? 4 : 8;  // bytes per sample
     // F blocks' gather windows (complex: (F-1)L + N samples; real: (2F-1)L + N floats) fit in
     // 8 F N bytes; +32 covers rounding the bulk copy out to 16-byte boundaries at both ends.
     // The same buffer then serves as the F padded exchange buffers (8 F xpad_len(N) bytes).
     static constexpr int EX_BYTES = 8 * F * xpad_len(N);
     static constexpr int BUF_BYTES = (((8 * F * N + 32) > EX_BYTES ? (8 * F * N + 32) : EX_BYTES) + 127) / 128 * 128;
-    static constexpr int H_BYTES = 8 * N;
-    static constexpr int SMEM_BYTES = 128 + H_BYTES + 2 * BUF_BYTES;
-    static constexpr int MIN_BLOCKS = THREADS <= 256 ? 2 : 1;
+    static constexpr int SMEM_BYTES = 128 + GROUPS * 3 * BUF_BYTES;
+    static constexpr int MIN_BLOCKS = 1;  // a CTA that allocates Tensor Memory runs alone on its SM
+    // Tensor Memory: per thread 32 columns of H bins + 32 per twiddled pass; warps w, w+4, ...
+    // share a lane range and take consecutive column ranges.
+    static constexpr int TM_COLS_THREAD = 32 * S::NPASS;
+    static constexpr int TM_SLOTS = THREADS / 128;
+    static constexpr int TM_NEED = TM_COLS_THREAD * TM_SLOTS;
+    static constexpr int TM_COLS =
+        TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128 : TM_NEED <= 256 ? 256 : 512;
+    static_assert(TM_NEED <= 512, "tensor memory columns");
+    static_assert(THREADS % 128 == 0, "whole warp quarters");
+    using Bar = GroupBarrier<GT>;
 };
 
 // Gather the input window of work unit u into `buf`.  Returns the element offset of
@@ -53,7 +74,8 @@ struct BlockCfg {
 // thread gathers with plain loads and the CTA synchronises (used_tma = false).
 template <int LOGN, bool REAL>
 __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsigned char *buf, uint64_t *bar,
-                                          bool allow_tma, bool &used_tma) {
+                                          bool allow_tma, bool &used_tma, int tid,
+                                          const typename BlockCfg<LOGN, REAL>::Bar &gbar) {
     using C = BlockCfg<LOGN, REAL>;
     constexpr int SB = C::SB;
     const int64_t span = (int64_t)C::F * p.L * (REAL ? 2 : 1);
@@ -64,7 +86,7 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
         const uintptr_t a0 = xb + (uintptr_t)start * SB, a1 = a0 + (uintptr_t)len * SB;
         const uintptr_t b0 = a0 & ~uintptr_t(15), b1 = (a1 + 15) & ~uintptr_t(15);
         if (b0 >= xb && b1 <= xb + (uintptr_t)p.n * SB) {
-            if (threadIdx.x == 0) {
+            if (tid == 0) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, (uint32_t)(b1 - b0));
                 bulk_g2s(buf, reinterpret_cast<const void *>(b0), (uint32_t)(b1 - b0), bar);
@@ -75,50 +97,35 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
     }
     used_tma = false;
     const int64_t hist = p.M - 1;
-    if constexpr (REAL) {
-        const float *x = static_cast<const float *>(p.x);
-        const float *s0 = static_cast<const float *>(p.state);
-        float *dst = reinterpret_cast<float *>(buf);
-        for (int64_t i = threadIdx.x; i < len; i += C::THREADS) {
-            const int64_t t = start + i;
-            float v = 0.f;
-            if (t >= 0) {
-                if (t < p.n) v = x[t];
-            } else if (t >= -hist) {
-                v = s0[hist + t];
-            }
-            dst[i] = v;
+    using T_ = typename std::conditional<REAL, float, float2>::type;
+    const T_ *x = static_cast<const T_ *>(p.x);
+    const T_ *s0 = static_cast<const T_ *>(p.state);
+    T_ *dst = reinterpret_cast<T_ *>(buf);
+    for (int64_t i = tid; i < len; i += C::GT) {
+        const int64_t t = start + i;
+        T_ v{};
+        if (t >= 0) {
+            if (t < p.n) v = x[t];
+        } else if (t >= -hist) {
+            v = s0[hist + t];
         }
-    } else {
-        const float2 *x = static_cast<const float2 *>(p.x);
-        const float2 *s0 = static_cast<const float2 *>(p.state);
-        float2 *dst = reinterpret_cast<float2 *>(buf);
-        for (int64_t i = threadIdx.x; i < len; i += C::THREADS) {
-            const int64_t t = start + i;
-            float2 v = make_float2(0.f, 0.f);
-            if (t >= 0) {
-                if (t < p.n) v = x[t];
-            } else if (t >= -hist) {
-                v = s0[hist + t];
-            }
-            dst[i] = v;
-        }
+        dst[i] = v;
     }
-    __syncthreads();
+    gbar.sync();
     return 0;
 }
 
 // S0' = xt[n-(M-1) .. n): samples of x, or (when n < M-1) of S0, which the gather of unit 0
 // left at buffer index (t + M - 1) for xt[t], t < 0.
 template <int LOGN, bool REAL>
-__device__ __forceinline__ void write_state(const BlockParams &p, const unsigned char *buf) {
+__device__ __forceinline__ void write_state(const BlockParams &p, const unsigned char *buf, int tid) {
     using C = BlockCfg<LOGN, REAL>;
     using T_ = typename std::conditional<REAL, float, float2>::type;
     const T_ *x = static_cast<const T_ *>(p.x);
     const T_ *stg = reinterpret_cast<const T_ *>(buf);
     T_ *st = static_cast<T_ *>(p.state);
     const int hist = p.M - 1;
-    for (int t = threadIdx.x; t < hist; t += C::THREADS) {
+    for (int t = tid; t < hist; t += C::GT) {
         const int64_t src = p.n - hist + t;
         st[t] = src >= 0 ? x[src] : stg[src + hist];
     }
@@ -128,96 +135,188 @@ template <int LOGN, bool REAL>
 __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, REAL>::MIN_BLOCKS)
     fos_block_kernel(const BlockParams p) {
     using C = BlockCfg<LOGN, REAL>;
+    using S = typename C::S;
     constexpr int T = C::T;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    float2 *hs = reinterpret_cast<float2 *>(smem + 128);  // H / N, natural order
-    unsigned char *bufs[2] = {smem + 128 + C::H_BYTES, smem + 128 + C::H_BYTES + C::BUF_BYTES};
     const int tid = threadIdx.x;
-    const int f = tid / T;  // transform slot within the CTA
-    const int j = tid % T;  // thread within the transform
+    const int warp = tid >> 5;
+    const int g = tid / C::GT;      // group within the CTA
+    const int tg = tid % C::GT;     // thread within the group
+    const int f = tg / T;           // transform slot within the group
+    const int j = tg % T;           // thread within the transform
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + 2 * g;
+    uint32_t *tm_base_slot = reinterpret_cast<uint32_t *>(smem + 64);
+    unsigned char *gbase = smem + 128 + g * 3 * C::BUF_BYTES;
+    float2 *xbuf = reinterpret_cast<float2 *>(gbase);  // exchange buffer
+    unsigned char *stg0 = gbase + C::BUF_BYTES;
+    unsigned char *stg1 = gbase + 2 * C::BUF_BYTES;
+    const typename C::Bar gbar{1 + g};
 
-    if (tid == 0) {
+    if (warp == 0) {
+        tmem_alloc(tm_base_slot, C::TM_COLS);
+        tmem_relinquish();
+    }
+    if (tg == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
-    // H / N stays in shared memory for every block this CTA filters
-    for (int i = tid; i < C::N; i += C::THREADS) hs[i] = __ldg(p.H + i);
+    tmem_fence_before_sync();
     __syncthreads();
+    tmem_fence_after_sync();
+    // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
+    const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
+                         (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+    {
+        // H[j + e T] / N for e = 0..15, then the twiddles W_{16 Ns}^{(j mod Ns) r} of each pass
+        float w[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float2 z = __ldg(p.H + j + (8 * h + e) * T);
+                w[2 * e] = z.x;
+                w[2 * e + 1] = z.y;
+            }
+            tmem_st16(tma + 16u * h, w);
+        }
+#pragma unroll
+        for (int q = 1; q < S::NPASS; ++q) {
+            const int Ns = S::ns(q);
+            const float2 *tw = p.tw + S::twoff(q) + (j & (Ns - 1));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 8 * h + e + 1;
+                    const float2 z = r < 16 ? __ldg(tw + (r - 1) * Ns) : make_float2(0.f, 0.f);
+                    w[2 * e] = z.x;
+                    w[2 * e + 1] = z.y;
+                }
+                tmem_st16(tma + 32u * q + 16u * h, w);
+            }
+        }
+        tmem_wait_st();
+    }
 
     // double buffering: `cur` holds the unit being filtered, `nxt` the one being fetched
-    unsigned char *cur = bufs[0], *nxt = bufs[1];
+    unsigned char *cur = stg0, *nxt = stg1;
     uint64_t *bcur = &bars[0], *bnxt = &bars[1];
     uint32_t pcur = 0u, pnxt = 0u;  // mbarrier phase parity to wait for
     bool ucur = false, unxt = false;  // filled by a bulk copy (else by plain loads)
     int ocur = 0, onxt = 0;           // element offset of the window in the buffer
     bool allow_tma = true;
 
-    int64_t u = blockIdx.x;
-    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur);
+    // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
+    const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
 
-    for (; u < p.nunits; u += gridDim.x) {
-        const int64_t un = u + gridDim.x;
-        if (un < p.nunits) onxt = stage_unit<LOGN, REAL>(p, un, nxt, bnxt, allow_tma, unxt);
+    // the groups of all CTAs take work units round-robin
+    const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
+    int64_t u = (int64_t)blockIdx.x * C::GROUPS + g;
+    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur, tg, gbar);
+
+    for (; u < p.nunits; u += stride) {
+        const int64_t un = u + stride;
+        if (un < p.nunits) onxt = stage_unit<LOGN, REAL>(p, un, nxt, bnxt, allow_tma, unxt, tg, gbar);
         if (ucur) {
             const bool ok = mbar_wait_bounded(bcur, pcur);
             pcur ^= 1u;
-            if (__syncthreads_or(!ok)) {
+            if (gbar.sync_or(!ok)) {
                 // the copy did not arrive in time: report it, stop using bulk copies and
                 // gather this unit with plain loads instead
-                if (tid == 0) atomicExch(p.err, 1);
+                if (tg == 0) atomicExch(p.err, 1);
                 allow_tma = false;
-                ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, false, ucur);
+                ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, false, ucur, tg, gbar);
             }
         }
 
         // gather E_i (step 3) from the staged window into registers: v[e] = E[j + e T]
         float2 v[16];
         if constexpr (REAL) {
-            const float *sr = reinterpret_cast<const float *>(cur) + ocur + 2 * f * p.L;
+            const float *sr = reinterpret_cast<const float *>(cur) + ocur + 2 * f * p.L + j;
+            const float *sr2 = sr + p.L;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = make_float2(sr[j + e * T], sr[p.L + j + e * T]);
+            for (int e = 0; e < 16; ++e) v[e] = make_float2(sr[e * T], sr2[e * T]);
         } else {
-            const float2 *sc = reinterpret_cast<const float2 *>(cur) + ocur + f * p.L;
+            const float2 *sc = reinterpret_cast<const float2 *>(cur) + ocur + f * p.L + j;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = sc[j + e * T];
+            for (int e = 0; e < 16; ++e) v[e] = sc[e * T];
         }
-        if (p.fuse_state && u == 0) write_state<LOGN, REAL>(p, cur);
-        __syncthreads();  // the window is consumed; the buffer becomes the exchange buffer
+        if (p.fuse_state && u == 0) write_state<LOGN, REAL>(p, cur, tg);
 
-        // step 4: FFT, multiply by H, IFFT
-        float2 *ex = reinterpret_cast<float2 *>(cur) + f * xpad_len(C::N);
-        fft_regs<LOGN, -1>(v, ex, p.tw, j, false);
+        // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
+        float2 *b0 = xbuf + f * xpad_len(C::N);
+        float2 *b1 = reinterpret_cast<float2 *>(cur) + f * xpad_len(C::N);
+        fft_tm<LOGN, false>(v, b0, b1, tma, j, gbar);
+        {
+            float h[16];
+            tmem_ld16(tma, h);
+            tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], hs[j + e * T]);
-        fft_regs<LOGN, +1>(v, ex, p.tw, j, true);
+            for (int e = 0; e < 8; ++e) v[e] = cmul(v[e], make_float2(h[2 * e], h[2 * e + 1]));
+            tmem_ld16(tma + 16u, h);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[8 + e] = cmul(v[8 + e], make_float2(h[2 * e], h[2 * e + 1]));
+        }
+        fft_tm<LOGN, true>(v, b0, b1, tma, j, gbar);
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
         const int64_t blk = REAL ? 2 * (u * C::F + f) : (u * C::F + f);
-        const int64_t obase = blk * p.L - (p.M - 1);
+        const int64_t o0 = blk * p.L - (p.M - 1) + j;  // output index of element e = 0
+        const bool whole = o0 + (int64_t)(15 * T) + (REAL ? p.L : 0) < p.n;
+        if constexpr (REAL) {
+            float *y = static_cast<float *>(p.y) + o0;
+            float *y2 = y + p.L;
+            if (whole) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int t = j + e * T;
-            if (t >= p.M - 1) {
-                const int64_t o = obase + t;
-                if constexpr (REAL) {
-                    float *y = static_cast<float *>(p.y);
-                    if (o < p.n) st_cs(y + o, v[e].x);
-                    if (o + p.L < p.n) st_cs(y + o + p.L, v[e].y);
-                } else {
-                    float2 *y = static_cast<float2 *>(p.y);
-                    if (o < p.n) st_cs(y + o, v[e]);
-                }
+                for (int e = 0; e < 16; ++e)
+                    if (e >= e_keep) {
+                        st_cs(y + e * T, v[e].x);
+                        st_cs(y2 + e * T, v[e].y);
+                    }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (e >= e_keep) {
+                        if (o0 + e * T < p.n) st_cs(y + e * T, v[e].x);
+                        if (o0 + e * T + p.L < p.n) st_cs(y2 + e * T, v[e].y);
+                    }
+            }
+        } else {
+            float2 *y = static_cast<float2 *>(p.y) + o0;
+            if (whole) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (e >= e_keep) st_cs(y + e * T, v[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (e >= e_keep && o0 + e * T < p.n) st_cs(y + e * T, v[e]);
             }
         }
-        __syncthreads();  // `cur` is free for the copy issued at the top of the next iteration
-        unsigned char *tb = cur; cur = nxt; nxt = tb;
-        uint64_t *tm = bcur; bcur = bnxt; bnxt = tm;
-        uint32_t tp = pcur; pcur = pnxt; pnxt = tp;
-        bool tu = ucur; ucur = unxt; unxt = tu;
-        int to = ocur; ocur = onxt; onxt = to;
+        gbar.sync();  // `cur` and the exchange buffer are free for the next unit
+        unsigned char *tb = cur;
+        cur = nxt;
+        nxt = tb;
+        uint64_t *tm = bcur;
+        bcur = bnxt;
+        bnxt = tm;
+        uint32_t tp = pcur;
+        pcur = pnxt;
+        pnxt = tp;
+        bool tu = ucur;
+        ucur = unxt;
+        unxt = tu;
+        int to = ocur;
+        ocur = onxt;
+        onxt = to;
     }
+
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    if (warp == 0) tmem_dealloc(*tm_base_slot, C::TM_COLS);
 }
 
 template <int LOGN, bool REAL>
@@ -229,6 +328,7 @@ KernelEntry block_entry() {
     k.smem = C::SMEM_BYTES;
     k.cluster = 1;
     k.units_per_cta = C::F;
+    k.groups = C::GROUPS;
     k.fft_logn = LOGN;
     return k;
 }

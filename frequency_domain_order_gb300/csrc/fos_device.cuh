@@ -20,8 +20,14 @@ namespace fos {
 
 // --------------------------------------------------------------------------- complex ops
 
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+// one packed f32x2 instruction per complex add / subtract
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+#else
 FOS_HD float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 FOS_HD float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+#endif
 FOS_HD float2 cneg(float2 a) { return make_float2(-a.x, -a.y); }
 
 // a * w
@@ -116,11 +122,17 @@ FOS_HD void dft2(float2 &a0, float2 &a1) {
 
 template <int DIR>
 FOS_HD void dft4(float2 &a0, float2 &a1, float2 &a2, float2 &a3) {
-    float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), t3 = crot<DIR>(csub(a1, a3));
+    const float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), t3 = csub(a1, a3);
     a0 = cadd(t0, t2);
     a2 = csub(t0, t2);
-    a1 = cadd(t1, t3);
-    a3 = csub(t1, t3);
+    // t1 +- (DIR i) t3, component by component (a quarter turn swaps re and im)
+    if constexpr (DIR < 0) {
+        a1 = make_float2(t1.x + t3.y, t1.y - t3.x);
+        a3 = make_float2(t1.x - t3.y, t1.y + t3.x);
+    } else {
+        a1 = make_float2(t1.x - t3.y, t1.y + t3.x);
+        a3 = make_float2(t1.x + t3.y, t1.y - t3.x);
+    }
 }
 
 // R = R1 * 4 with n = 4 a + b, k = c + R1 d:
@@ -263,5 +275,73 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_smem_addr, uint32_t 
 __device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }
+
+// --------------------------------------------------------------------------- tensor memory
+// Tensor Memory (TMEM) used as per-thread storage for values that stay constant while a CTA
+// lives (the response H and the pass twiddles): 128 lanes x 512 32-bit columns per SM; warp w
+// of a CTA reaches lanes 32 (w % 4) .. 32 (w % 4) + 31, and with the 32x32b shape thread t of
+// the warp reads its own lane.  Allocation is by one whole warp; the CTA frees it before exit.
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive columns of this thread's lane <-> 16 registers
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]),
+          "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7]), "f"(r[8]), "f"(r[9]),
+        "f"(r[10]), "f"(r[11]), "f"(r[12]), "f"(r[13]), "f"(r[14]), "f"(r[15])
+        : "memory");
+}
+
+// --------------------------------------------------------------------------- group barriers
+// A CTA may run several independent thread groups; each synchronises on its own hardware
+// barrier (id >= 1; id 0 is __syncthreads).  NT = threads in the group (a multiple of 32).
+template <int NT>
+struct GroupBarrier {
+    int id;
+    __device__ __forceinline__ void sync() const {
+        asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NT) : "memory");
+    }
+    // barrier that also returns whether `pred` was true in any thread of the group
+    __device__ __forceinline__ bool sync_or(bool pred) const {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.or.pred q, %2, %3, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"((uint32_t)pred), "r"(id), "n"(NT)
+            : "memory");
+        return r != 0;
+    }
+};
 
 }  // namespace fos

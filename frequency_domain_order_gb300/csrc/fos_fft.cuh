@@ -90,4 +90,96 @@ __device__ __forceinline__ void fft_regs(float2 (&v)[16], float2 *ex, const floa
     fft_pass<LOGN, DIR, 1>(v, ex, tw, j);
 }
 
+// ---------------------------------------------------------------------------------------
+// Variant for the single-CTA kernel: twiddles come from Tensor Memory (this thread's lane,
+// 32 columns per pass at tw_taddr + 32 p: entry r-1 of pass p at columns 2(r-1), 2(r-1)+1),
+// and the passes alternate between two exchange buffers, so each pass needs one barrier
+// instead of two.  Pass p of the forward transform (INV = false) writes buffer (p mod 2) and
+// reads buffer ((p-1) mod 2); the inverse transform is shifted by NPASS + 1 so that its first
+// write never lands in the buffer the forward transform's last pass reads.  Every buffer is
+// xpad_len(N) elements of this transform.
+
+template <int LOGN, int P, bool INV, class Bar>
+__device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, uint32_t tw_taddr, int j,
+                                            const Bar &bar) {
+    using S = FftShape<LOGN>;
+    if constexpr (P < S::NPASS) {
+        constexpr int T = S::T;
+        constexpr int Ns = S::ns(P);
+        constexpr bool last = (P == S::NPASS - 1);
+        constexpr int DIR = INV ? 1 : -1;
+        constexpr int SH = INV ? S::NPASS + 1 : 0;
+        float2 *rd = ((P - 1 + SH) % 2 == 0) ? b0 : b1;
+        float2 *wr = ((P + SH) % 2 == 0) ? b0 : b1;
+        if constexpr (T % 16 == 0) {
+            const float2 *src = rd + xpad(j);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = src[e * xpad_len(T)];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = rd[xpad(j + e * T)];
+        }
+        float tw[16];
+        tmem_ld16(tw_taddr + 32u * P, tw);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 1; r <= 8; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 2], tw[2 * r - 1]));
+        tmem_ld16(tw_taddr + 32u * P + 16u, tw);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
+        dft<16, DIR>(v);
+        if constexpr (!last) {
+            const int m = j & (Ns - 1);
+            const int base = (j / Ns) * (16 * Ns) + m;
+            if constexpr (Ns % 16 == 0) {
+                float2 *dst = wr + xpad(base);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) dst[r * xpad_len(Ns)] = v[r];
+            } else {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) wr[xpad(base + r * Ns)] = v[r];
+            }
+            bar.sync();
+        }
+        fft_tm_pass<LOGN, P + 1, INV>(v, b0, b1, tw_taddr, j, bar);
+    }
+}
+
+// Transform v in place (layout z[j + e T] -> Z[j + e T]).  `bar` synchronises the threads that
+// share the two buffers.  No barrier is needed before the first write: see the buffer rotation
+// above and the callers' barrier placement.
+template <int LOGN, bool INV, class Bar>
+__device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, uint32_t tw_taddr, int j,
+                                       const Bar &bar) {
+    using S = FftShape<LOGN>;
+    constexpr int T = S::T, R0 = S::R0, G = 16 / R0;
+    constexpr int DIR = INV ? 1 : -1;
+    constexpr int SH = INV ? S::NPASS + 1 : 0;
+    float2 *wr = (SH % 2 == 0) ? b0 : b1;
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+        float2 a[R0];
+#pragma unroll
+        for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
+        dft<R0, DIR>(a);
+#pragma unroll
+        for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
+    }
+    if constexpr ((T * R0) % 16 == 0) {
+        float2 *dst = wr + j * R0 + ((j * R0) >> 4);
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+#pragma unroll
+            for (int r = 0; r < R0; ++r) dst[q * (T * R0 + (T * R0) / 16) + r] = v[q + r * G];
+    } else {
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+#pragma unroll
+            for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
+    }
+    bar.sync();
+    fft_tm_pass<LOGN, 1, INV>(v, b0, b1, tw_taddr, j, bar);
+}
+
 }  // namespace fos

@@ -28,6 +28,7 @@ struct KernelEntry {
     int smem = 0;                // dynamic shared memory per CTA (bytes)
     int cluster = 1;             // CTAs per cluster (1 = no cluster)
     int units_per_cta = 1;       // blocks (complex) or block pairs (real) per work unit
+    int groups = 1;              // independent thread groups per CTA, each taking work units
     int fft_logn = 0;            // log2 of the per-CTA transform size (twiddle table shape)
 };
 
