@@ -101,15 +101,25 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
     const T_ *x = static_cast<const T_ *>(p.x);
     const T_ *s0 = static_cast<const T_ *>(p.state);
     T_ *dst = reinterpret_cast<T_ *>(buf);
-    for (int64_t i = tid; i < len; i += C::GT) {
-        const int64_t t = start + i;
-        T_ v{};
-        if (t >= 0) {
-            if (t < p.n) v = x[t];
-        } else if (t >= -hist) {
-            v = s0[hist + t];
+    // batches of independent loads, so their latencies overlap instead of adding up
+    constexpr int U = 8;
+    for (int64_t i0 = tid; i0 < len; i0 += (int64_t)U * C::GT) {
+        T_ v[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int64_t t = start + i0 + (int64_t)q * C::GT;
+            v[q] = T_{};
+            if (t >= 0) {
+                if (t < p.n) v[q] = x[t];
+            } else if (t >= -hist) {
+                v[q] = s0[hist + t];
+            }
         }
-        dst[i] = v;
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int64_t i = i0 + (int64_t)q * C::GT;
+            if (i < len) dst[i] = v[q];
+        }
     }
     gbar.sync();
     return 0;
@@ -125,9 +135,19 @@ __device__ __forceinline__ void write_state(const BlockParams &p, const unsigned
     const T_ *stg = reinterpret_cast<const T_ *>(buf);
     T_ *st = static_cast<T_ *>(p.state);
     const int hist = p.M - 1;
-    for (int t = tid; t < hist; t += C::GT) {
-        const int64_t src = p.n - hist + t;
-        st[t] = src >= 0 ? x[src] : stg[src + hist];
+    constexpr int U = 8;  // independent loads in flight per thread
+    for (int t0 = tid; t0 < hist; t0 += U * C::GT) {
+        T_ v[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int t = t0 + q * C::GT;
+            const int64_t src = p.n - hist + t;
+            v[q] = T_{};
+            if (t < hist) v[q] = src >= 0 ? x[src] : stg[src + hist];
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q)
+            if (t0 + q * C::GT < hist) st[t0 + q * C::GT] = v[q];
     }
 }
 
@@ -164,41 +184,6 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
-    // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
-    const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
-                         (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
-    {
-        // H[j + e T] / N for e = 0..15, then the twiddles W_{16 Ns}^{(j mod Ns) r} of each pass
-        float w[16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float2 z = __ldg(p.H + j + (8 * h + e) * T);
-                w[2 * e] = z.x;
-                w[2 * e + 1] = z.y;
-            }
-            tmem_st16(tma + 16u * h, w);
-        }
-#pragma unroll
-        for (int q = 1; q < S::NPASS; ++q) {
-            const int Ns = S::ns(q);
-            const float2 *tw = p.tw + S::twoff(q) + (j & (Ns - 1));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = 8 * h + e + 1;
-                    const float2 z = r < 16 ? __ldg(tw + (r - 1) * Ns) : make_float2(0.f, 0.f);
-                    w[2 * e] = z.x;
-                    w[2 * e + 1] = z.y;
-                }
-                tmem_st16(tma + 32u * q + 16u * h, w);
-            }
-        }
-        tmem_wait_st();
-    }
-
     // double buffering: `cur` holds the unit being filtered, `nxt` the one being fetched
     unsigned char *cur = stg0, *nxt = stg1;
     uint64_t *bcur = &bars[0], *bnxt = &bars[1];
@@ -207,13 +192,52 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     int ocur = 0, onxt = 0;           // element offset of the window in the buffer
     bool allow_tma = true;
 
-    // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
-    const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
-
-    // the groups of all CTAs take work units round-robin
+    // the groups of all CTAs take work units round-robin; the first unit's copy is started
+    // before the Tensor Memory set-up so that the two latencies overlap
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
     int64_t u = (int64_t)blockIdx.x * C::GROUPS + g;
     if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur, tg, gbar);
+
+    // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
+    const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
+                         (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+    {
+        // H[j + e T] / N for e = 0..15, then the twiddles W_{16 Ns}^{(j mod Ns) r} of each pass;
+        // every load is issued before the first store into TMEM
+        float w[S::NPASS][32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float2 z = __ldg(p.H + j + e * T);
+            w[0][2 * e] = z.x;
+            w[0][2 * e + 1] = z.y;
+        }
+#pragma unroll
+        for (int q = 1; q < S::NPASS; ++q) {
+            const int Ns = S::ns(q);
+            const float2 *tw = p.tw + S::twoff(q) + (j & (Ns - 1));
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                const float2 z = __ldg(tw + (r - 1) * Ns);
+                w[q][2 * r - 2] = z.x;
+                w[q][2 * r - 1] = z.y;
+            }
+            w[q][30] = 0.f;
+            w[q][31] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < S::NPASS; ++q)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float c[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) c[k] = w[q][16 * h + k];
+                tmem_st16(tma + 32u * q + 16u * h, c);
+            }
+        tmem_wait_st();
+    }
+
+    // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
+    const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
 
     for (; u < p.nunits; u += stride) {
         const int64_t un = u + stride;

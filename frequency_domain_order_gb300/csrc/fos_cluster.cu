@@ -94,17 +94,30 @@ __device__ __forceinline__ void cluster_stage(const BlockParams &p, int64_t u, u
     using T_ = typename std::conditional<REAL, float, float2>::type;
     const T_ *x = static_cast<const T_ *>(p.x);
     const T_ *s0 = static_cast<const T_ *>(p.state);
-    for (int i = threadIdx.x; i < nb * C * Q; i += C_::T) {
-        const int run = i / Q, k = i % Q;  // run = blockhalf * C + a
-        const int a = run % C, half = run / C;
-        const int64_t t = s + (int64_t)half * p.L + (int64_t)a * P + k;
-        T_ v{};
-        if (t >= 0) {
-            if (t < p.n) v = x[t];
-        } else if (t >= -hist) {
-            v = s0[hist + t];
+    // batches of independent loads, so their latencies overlap instead of adding up
+    constexpr int U = 8;
+    for (int i0 = threadIdx.x; i0 < nb * C * Q; i0 += U * C_::T) {
+        T_ v[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int i = i0 + q * C_::T;
+            const int run = i / Q, k = i % Q;  // run = blockhalf * C + a
+            const int a = run % C, half = run / C;
+            const int64_t t = s + (int64_t)half * p.L + (int64_t)a * P + k;
+            v[q] = T_{};
+            if (i < nb * C * Q) {
+                if (t >= 0) {
+                    if (t < p.n) v[q] = x[t];
+                } else if (t >= -hist) {
+                    v[q] = s0[hist + t];
+                }
+            }
         }
-        reinterpret_cast<T_ *>(stg + run * C_::SEG_BYTES)[k] = v;
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int i = i0 + q * C_::T;
+            if (i < nb * C * Q) reinterpret_cast<T_ *>(stg + (i / Q) * C_::SEG_BYTES)[i % Q] = v[q];
+        }
     }
     __syncthreads();
 }
