@@ -16,7 +16,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/fir_os.h"
+#include "fir_os.h"  // include/ is on the include path (build.py)
 #include "fos_fft.cuh"
 #include "fos_kernels.h"
 

@@ -58,7 +58,7 @@ struct BlockCfg {
     static constexpr int MIN_BLOCKS = 1;  // a CTA that allocates Tensor Memory runs alone on its SM
     // Tensor Memory: per thread 32 columns of H bins + 32 per twiddled pass; warps w, w+4, ...
     // share a lane range and take consecutive column ranges.
-    static constexpr int TM_COLS_THREAD = 32 * S::NPASS;
+    static constexpr int TM_COLS_THREAD = TwLayout<LOGN, 0>::TMEM_COLS;  // = 32 NPASS
     static constexpr int TM_SLOTS = THREADS / 128;
     static constexpr int TM_NEED = TM_COLS_THREAD * TM_SLOTS;
     static constexpr int TM_COLS =
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
         float2 *b1 = reinterpret_cast<float2 *>(cur) + f * xpad_len(C::N);
-        fft_tm<LOGN, false>(v, b0, b1, tma, j, gbar);
+        fft_tm<LOGN, 0, false>(v, b0, b1, nullptr, tma, j, gbar);
         {
             float h[16];
             tmem_ld16(tma, h);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[8 + e] = cmul(v[8 + e], make_float2(h[2 * e], h[2 * e + 1]));
         }
-        fft_tm<LOGN, true>(v, b0, b1, tma, j, gbar);
+        fft_tm<LOGN, 0, true>(v, b0, b1, nullptr, tma, j, gbar);
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
         const int64_t blk = REAL ? 2 * (u * C::F + f) : (u * C::F + f);

@@ -38,6 +38,31 @@ struct FftShape {
     static_assert(LOGN >= 6 && LOGN <= 13, "one CTA holds 64 .. 8192 points");
 };
 
+// Where the twiddles of each pass of the Tensor-Memory variant below live: passes with
+// Ns <= SMAX read a small shared-memory table (entry r-1 of pass p at
+// smem_off(p) + (r-1) Ns + m, m = j mod Ns), the others 32 Tensor-Memory columns of the thread's
+// lane starting at tmem_col(p) (entry r-1 at columns 2(r-1), 2(r-1)+1).  Columns 0..31 hold the
+// thread's 16 bins of H; TMEM_COLS is the first column after the twiddles.
+template <int LOGN, int SMAX>
+struct TwLayout {
+    using S = FftShape<LOGN>;
+    __host__ __device__ static constexpr bool in_smem(int p) { return S::ns(p) <= SMAX; }
+    __host__ __device__ static constexpr int smem_off(int p) {
+        int o = 0;
+        for (int q = 1; q < p; ++q)
+            if (in_smem(q)) o += 15 * S::ns(q);
+        return o;
+    }
+    __host__ __device__ static constexpr int tmem_col(int p) {
+        int c = 32;
+        for (int q = 1; q < p; ++q)
+            if (!in_smem(q)) c += 32;
+        return c;
+    }
+    static constexpr int SMEM_ENTRIES = smem_off(S::NPASS);
+    static constexpr int TMEM_COLS = tmem_col(S::NPASS);
+};
+
 template <int LOGN, int DIR, int P>
 __device__ __forceinline__ void fft_pass(float2 (&v)[16], float2 *ex, const float2 *__restrict__ tw, int j) {
     using S = FftShape<LOGN>;
@@ -91,17 +116,23 @@ __device__ __forceinline__ void fft_regs(float2 (&v)[16], float2 *ex, const floa
 }
 
 // ---------------------------------------------------------------------------------------
-// Variant for the single-CTA kernel: twiddles come from Tensor Memory (this thread's lane,
-// 32 columns per pass at tw_taddr + 32 p: entry r-1 of pass p at columns 2(r-1), 2(r-1)+1),
-// and the passes alternate between two exchange buffers, so each pass needs one barrier
-// instead of two.  Pass p of the forward transform (INV = false) writes buffer (p mod 2) and
-// reads buffer ((p-1) mod 2); the inverse transform is shifted by NPASS + 1 so that its first
-// write never lands in the buffer the forward transform's last pass reads.  Every buffer is
+// Variant with per-thread twiddles in Tensor Memory (or, for passes with Ns <= SMAX, in the
+// shared table `stw`), laid out as TwLayout<LOGN, SMAX> describes.  The passes alternate between two
+// exchange buffers, so each pass needs one barrier: pass p of the forward transform
+// (INV = false) writes buffer (p mod 2) and reads buffer ((p-1) mod 2); the inverse transform
+// is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
+// transform's last pass reads.  `hook()` runs once, at the start of the last pass, after the
+// barrier that ended the pass before it; the inverse transform's last pass reads only b1, so
+// from there on b0 is free (a caller can start its next copy into it).  Every buffer is
 // xpad_len(N) elements of this transform.
 
-template <int LOGN, int P, bool INV, class Bar>
-__device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, uint32_t tw_taddr, int j,
-                                            const Bar &bar) {
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+template <int LOGN, int SMAX, int P, bool INV, class Bar, class Hook>
+__device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
+                                            uint32_t tm, int j, const Bar &bar, const Hook &hook) {
     using S = FftShape<LOGN>;
     if constexpr (P < S::NPASS) {
         constexpr int T = S::T;
@@ -109,6 +140,7 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
         constexpr bool last = (P == S::NPASS - 1);
         constexpr int DIR = INV ? 1 : -1;
         constexpr int SH = INV ? S::NPASS + 1 : 0;
+        if constexpr (last) hook();
         float2 *rd = ((P - 1 + SH) % 2 == 0) ? b0 : b1;
         float2 *wr = ((P + SH) % 2 == 0) ? b0 : b1;
         if constexpr (T % 16 == 0) {
@@ -119,18 +151,25 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = rd[xpad(j + e * T)];
         }
-        float tw[16];
-        tmem_ld16(tw_taddr + 32u * P, tw);
-        tmem_wait_ld();
+        const int m = j & (Ns - 1);
+        using TL = TwLayout<LOGN, SMAX>;
+        if constexpr (TL::in_smem(P)) {
+            const float2 *t = stw + TL::smem_off(P) + m;
 #pragma unroll
-        for (int r = 1; r <= 8; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 2], tw[2 * r - 1]));
-        tmem_ld16(tw_taddr + 32u * P + 16u, tw);
-        tmem_wait_ld();
+            for (int r = 1; r < 16; ++r) v[r] = ctw<DIR>(v[r], t[(r - 1) * Ns]);
+        } else {
+            float tw[16];
+            tmem_ld16(tm + (uint32_t)TL::tmem_col(P), tw);
+            tmem_wait_ld();
 #pragma unroll
-        for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
+            for (int r = 1; r <= 8; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 2], tw[2 * r - 1]));
+            tmem_ld16(tm + (uint32_t)TL::tmem_col(P) + 16u, tw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
+        }
         dft<16, DIR>(v);
         if constexpr (!last) {
-            const int m = j & (Ns - 1);
             const int base = (j / Ns) * (16 * Ns) + m;
             if constexpr (Ns % 16 == 0) {
                 float2 *dst = wr + xpad(base);
@@ -142,16 +181,16 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, P + 1, INV>(v, b0, b1, tw_taddr, j, bar);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV>(v, b0, b1, stw, tm, j, bar, hook);
     }
 }
 
 // Transform v in place (layout z[j + e T] -> Z[j + e T]).  `bar` synchronises the threads that
 // share the two buffers.  No barrier is needed before the first write: see the buffer rotation
 // above and the callers' barrier placement.
-template <int LOGN, bool INV, class Bar>
-__device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, uint32_t tw_taddr, int j,
-                                       const Bar &bar) {
+template <int LOGN, int SMAX, bool INV, class Bar, class Hook = NoHook>
+__device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
+                                       int j, const Bar &bar, const Hook &hook = Hook()) {
     using S = FftShape<LOGN>;
     constexpr int T = S::T, R0 = S::R0, G = 16 / R0;
     constexpr int DIR = INV ? 1 : -1;
@@ -179,7 +218,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, 1, INV>(v, b0, b1, tw_taddr, j, bar);
+    fft_tm_pass<LOGN, SMAX, 1, INV>(v, b0, b1, stw, tm, j, bar, hook);
 }
 
 }  // namespace fos
