@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     uint32_t pcur = 0u, pnxt = 0u;  // mbarrier phase parity to wait for
     bool ucur = false, unxt = false;  // filled by a bulk copy (else by plain loads)
     int ocur = 0, onxt = 0;           // element offset of the window in the buffer
-    bool allow_tma = true;
+    bool allow_tma = !p.no_bulk;  // bulk copies read device memory only
 
     // the groups of all CTAs take work units round-robin; the first unit's copy is started
     // before the Tensor Memory set-up so that the two latencies overlap

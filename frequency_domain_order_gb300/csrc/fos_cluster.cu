@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256, 2) fos_cluster_kernel(const BlockParams p
     cluster_sync();  // every CTA of the cluster is running before any remote store
 
     uint32_t parity = 0u;
-    bool used = false, allow_tma = true;
+    bool used = false, allow_tma = !p.no_bulk;  // bulk copies read device memory only
     int offA = 0, offB = 0;
     int64_t u = cid;
     if (u < p.nunits) cluster_stage<LOGN, REAL>(p, u, rank, stg, bar, allow_tma, used, offA, offB);

@@ -20,6 +20,7 @@ struct BlockParams {
     int M;                 // taps
     int L;                 // block length N - M + 1
     int fuse_state;        // the kernel writes S0' itself (else a state kernel follows)
+    int no_bulk;           // gather every unit with plain loads (x in page-locked host memory)
 };
 
 struct KernelEntry {

@@ -106,20 +106,21 @@ int fir_os_execute(fir_os_plan_t plan, const void *x_dev, int64_t n_samples, voi
 
 /*
  * fir_os_execute_host -- the same filtering for input and output in HOST memory: step 2
- * and step 6 of the claim (copy a chunk in, filter it, copy the result out, repeat while
- * data remains), pipelined over two device buffer sets so that the copies of one chunk
- * overlap the filtering of the next.  Synchronous: returns when y_host and state_host
- * hold the results.
+ * and step 6 of the claim (move a chunk to the GPU, filter it, move the result back, repeat
+ * while data remains).  Synchronous: returns when y_host and state_host hold the results.
  *
- *   x_host, y_host   n_samples samples each, host memory (page-locked memory gives
- *                    asynchronous copies; pageable memory works but serialises them)
+ *   x_host, y_host   n_samples samples each, host memory
  *   state_host       M-1 samples in/out (host), as for fir_os_execute; NULL only if M == 1
  *   stream           the caller's stream; work is ordered after it and it is synchronised
  *
- * The plan allocates its device buffers for this call on first use (two input and two
- * output chunks of about 2^21 samples, a whole number of blocks, so the chunks cut the stream
- * at the same block boundaries as one fir_os_execute call) and keeps them until
- * fir_os_plan_destroy.
+ * When x, y and the state are all page-locked (cudaHostAlloc / cudaHostRegister, e.g. torch
+ * pin_memory), the kernel reads x and writes y and the state in place over the host link: no
+ * staging copies.  Otherwise the call copies chunks of about 2^21 samples (a whole number of
+ * transforms -- blocks, or block pairs for real data -- so the chunks cut the stream where one
+ * fir_os_execute call's transforms begin) through two device buffer sets, pipelined over three
+ * streams so that the copies of one chunk overlap the filtering of the next; the plan allocates
+ * those buffers on first use and keeps them until fir_os_plan_destroy.  Either way the results
+ * equal fir_os_execute's, bit for bit.
  */
 int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n_samples,
                         void *y_host, void *state_host, void *stream);
