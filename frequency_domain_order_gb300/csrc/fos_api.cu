@@ -91,6 +91,15 @@ __global__ void fos_scale_h(const float2 *Hin, float2 *H, int N) {
     }
 }
 
+// Hk[c (N / C) + d] = H[c + C d]: the c-major order of the resident kernel.
+__global__ void fos_permute_h(const float2 *H, float2 *Hk, int N, int C) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < N) {
+        const int P = N / C;
+        Hk[t] = H[(t % P) * C + t / P];
+    }
+}
+
 // S0' = last M-1 samples of concat(S0, x), in place, one CTA.  Used when the block kernel
 // cannot write the state itself (more than one work unit reads S0).  For n < M-1 the kept
 // part of S0 moves towards the front; chunks are read completely before they are written and
@@ -163,6 +172,7 @@ struct fir_os_plan {
     fos::KernelEntry kernel;
     int max_units_in_flight = 0;  // CTAs (single-CTA kernel) or clusters (cluster kernel)
     float2 *d_H = nullptr;
+    float2 *d_Hk = nullptr;  // H in the kernel's order, when that is not the natural one
     float2 *d_tw = nullptr;
     float2 *d_twa = nullptr;
     int *d_err = nullptr;
@@ -183,6 +193,7 @@ int sample_bytes(const fir_os_plan *p) { return p->data_kind == FIR_OS_REAL ? 4 
 void free_plan(fir_os_plan *p) {
     if (!p) return;
     cudaFree(p->d_H);
+    cudaFree(p->d_Hk);
     cudaFree(p->d_tw);
     cudaFree(p->d_twa);
     cudaFree(p->d_err);
@@ -246,12 +257,12 @@ int64_t units_for(const fir_os_plan *p, int64_t n) {
 }
 
 // The block kernel writes S0' itself when only its first work unit reads S0 (the next unit
-// starts at or after sample 0); the cluster kernel additionally needs n >= M-1, because its
-// copy of S0 is spread over the cluster's CTAs.
+// starts at or after sample 0); the cluster and resident kernels additionally need n >= M-1,
+// because they write S0' from x (they keep no staged copy of S0).
 bool fuse_state(const fir_os_plan *p, int64_t n) {
     if (p->M == 1) return true;
     const int64_t span = (int64_t)p->kernel.units_per_cta * p->L * (p->data_kind == FIR_OS_REAL ? 2 : 1);
-    if (p->kernel.cluster == 1) return span >= p->M - 1;
+    if (p->kernel.cluster == 1 && !p->kernel.state_from_x) return span >= p->M - 1;
     return span >= p->M - 1 && n >= p->M - 1;
 }
 
@@ -262,7 +273,7 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.x = x;
     bp.y = y;
     bp.state = state;
-    bp.H = p->d_H;
+    bp.H = p->d_Hk ? p->d_Hk : p->d_H;
     bp.tw = p->d_tw;
     bp.twa = p->d_twa;
     bp.err = p->d_err;
@@ -396,6 +407,7 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
     const bool real = data_kind == FIR_OS_REAL;
     if (logn <= 9) p->kernel = fos::block_kernel_small(logn, real);
     else if (logn <= 13) p->kernel = fos::block_kernel_large(logn, real);
+    else if (logn <= 15) p->kernel = fos::resident_kernel(logn, real);
     else p->kernel = fos::cluster_kernel(logn, real);
     if (!p->kernel.func) return bail(fail(FIR_OS_E_UNSUPPORTED, "no kernel for N = %d", N));
 
@@ -450,6 +462,26 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
         if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice,
                                  stream)) != cudaSuccess)
             return bail(cuda_fail(e, "twiddle upload"));
+        if (p->kernel.split_c > 0) {
+            // W_N^{rc} (r < 128, c < C) and W_N^{128 k} (k < N / 128), float64 then rounded
+            const int C = p->kernel.split_c, HI = N / 128;
+            std::vector<float2> twa((size_t)(C * 128 + HI));
+            for (int c = 0; c < C; ++c)
+                for (int r = 0; r < 128; ++r) {
+                    const double ang = -2.0 * M_PI * (double)(r * c) / (double)N;
+                    twa[(size_t)c * 128 + r] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+                }
+            for (int k = 0; k < HI; ++k) {
+                const double ang = -2.0 * M_PI * (double)k / (double)HI;
+                twa[(size_t)C * 128 + k] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+            if ((e = cudaMalloc(&p->d_twa, sizeof(float2) * twa.size())) != cudaSuccess)
+                return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(split twiddles) failed"));
+            if ((e = cudaMemcpyAsync(p->d_twa, twa.data(), sizeof(float2) * twa.size(), cudaMemcpyHostToDevice,
+                                     stream)) != cudaSuccess)
+                return bail(cuda_fail(e, "split twiddle upload"));
+            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
+        }
         if (p->kernel.cluster > 1) {
             const int P = 1 << p->kernel.fft_logn, C = N / P;
             std::vector<float2> twa((size_t)N);
@@ -518,6 +550,14 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
                                  dev, hmax));
         }
     }
+    if (p->kernel.split_c > 0) {
+        // the resident kernel reads H[c + C d] for one c at a time: store it c-major
+        cudaError_t e = cudaMalloc(&p->d_Hk, sizeof(float2) * N);
+        if (e != cudaSuccess) return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(H, c-major) failed"));
+        fos_permute_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(p->d_H, p->d_Hk, N, p->kernel.split_c);
+        if ((e = cudaGetLastError()) != cudaSuccess) return bail(cuda_fail(e, "H permute kernel"));
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "H permute sync"));
+    }
     (void)rc;
     *out = p;
     return FIR_OS_OK;
@@ -540,7 +580,7 @@ int fir_os_plan_info(fir_os_plan_t plan, int *M, int *N, int *L) {
 
 int fir_os_plan_kernel(fir_os_plan_t plan, int *kind, int *cluster_size, int *grid, int *smem_bytes) {
     if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
-    if (kind) *kind = plan->kernel.cluster > 1 ? 1 : 0;
+    if (kind) *kind = plan->kernel.cluster > 1 ? 1 : plan->kernel.split_c > 0 ? 2 : 0;
     if (cluster_size) *cluster_size = plan->kernel.cluster;
     if (grid) *grid = plan->max_units_in_flight * plan->kernel.cluster;
     if (smem_bytes) *smem_bytes = plan->kernel.smem;

@@ -239,6 +239,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Hint: bring [src, src + bytes) of global memory into L2 (no completion to wait for).
+// src 16-byte aligned, bytes a multiple of 16; the range must lie inside one allocation.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // streaming (evict-first) global stores
 __device__ __forceinline__ void st_cs(float2 *p, float2 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_cs(float *p, float v) { __stcs(p, v); }
@@ -277,10 +283,11 @@ __device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
 }
 
 // --------------------------------------------------------------------------- tensor memory
-// Tensor Memory (TMEM) used as per-thread storage for values that stay constant while a CTA
-// lives (the response H and the pass twiddles): 128 lanes x 512 32-bit columns per SM; warp w
+// Tensor Memory (TMEM) used as per-thread storage: 128 lanes x 512 32-bit columns per SM; warp w
 // of a CTA reaches lanes 32 (w % 4) .. 32 (w % 4) + 31, and with the 32x32b shape thread t of
-// the warp reads its own lane.  Allocation is by one whole warp; the CTA frees it before exit.
+// the warp reads its own lane, so the threads t, t + 128, t + 256, ... of a CTA share a lane.
+// The block kernels keep constants there (the response H and the pass twiddles), the resident
+// kernel a whole block.  Allocation is by one whole warp; the CTA frees it before exit.
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
@@ -318,6 +325,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) 
         "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7]), "f"(r[8]), "f"(r[9]),
         "f"(r[10]), "f"(r[11]), "f"(r[12]), "f"(r[13]), "f"(r[14]), "f"(r[15])
         : "memory");
+}
+
+// Two complex values (four columns) of this thread's lane.  No memory clobber: Tensor Memory is
+// not addressable by ordinary loads and stores, so these may move across them (ordering
+// against tcgen05.wait / fences, which are volatile too, is kept).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float2 &a, float2 &b) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(a.x), "=f"(a.y), "=f"(b.x), "=f"(b.y)
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, float2 a, float2 b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "f"(a.x), "f"(a.y),
+                 "f"(b.x), "f"(b.y));
 }
 
 // --------------------------------------------------------------------------- group barriers

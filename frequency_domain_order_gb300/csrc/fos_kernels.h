@@ -11,9 +11,11 @@ struct BlockParams {
     const void *x;         // n input samples (float or float2)
     void *y;               // n output samples
     void *state;           // M-1 samples of S0 in, S0' out (NULL when M == 1)
-    const float2 *H;       // N bins, H / N, natural order
+    const float2 *H;       // N bins, H / N: natural order, or c-major (H[c + C d] at [c P + d])
+                           // for the resident kernel
     const float2 *tw;      // Stockham pass twiddles of the per-CTA transform
-    const float2 *twa;     // cluster kernel: W_N^{b c} at [c * P + b]
+    const float2 *twa;     // cluster kernel: W_N^{b c} at [c * P + b]; resident kernel:
+                           // W_N^{r c} at [c * 128 + r], then W_N^{128 k} at [C * 128 + k]
     int *err;              // device error word (set to 1 when a bounded wait ran out)
     int64_t n;             // samples in this call
     int64_t nunits;        // work units (block groups / blocks / block pairs)
@@ -31,6 +33,8 @@ struct KernelEntry {
     int units_per_cta = 1;       // blocks (complex) or block pairs (real) per work unit
     int groups = 1;              // independent thread groups per CTA, each taking work units
     int fft_logn = 0;            // log2 of the per-CTA transform size (twiddle table shape)
+    int split_c = 0;             // resident kernel: C = N / 2^fft_logn (H c-major, twa as above)
+    int state_from_x = 0;        // the fused state write reads x only (needs n >= M - 1)
 };
 
 // Single-CTA kernels, N = 2^logn, logn in [6, 13].
@@ -38,6 +42,8 @@ KernelEntry block_kernel_small(int logn, bool real);   // logn 6..9
 KernelEntry block_kernel_large(int logn, bool real);   // logn 10..13
 // Cluster kernels, N = 2^logn, logn in [14, 16].
 KernelEntry cluster_kernel(int logn, bool real);
+// One block resident in one SM's Tensor Memory, N = 2^logn, logn in [14, 15].
+KernelEntry resident_kernel(int logn, bool real);
 
 // Entries of the pass-twiddle table for a per-CTA transform of 2^logn points.
 int pass_twiddle_entries(int logn);

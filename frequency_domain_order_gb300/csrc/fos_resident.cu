@@ -1,0 +1,335 @@
+// fos_resident.cu -- the fused overlap-save block kernel for N = 16384 and 32768: one block
+// resident in one SM's Tensor Memory.
+//
+// Steps 3-5 of the claim in "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法"
+// (zl.czvv.com/42398539.html, 主权项) for N = C x P, P = 4096, C = N / P (4 or 8), computed
+// with the split n = P a + b, k = c + C d of the DFT:
+//
+//   X[c + C d] = sum_b W_P^{bd} [ W_N^{bc} sum_a x[P a + b] W_C^{ac} ]
+//   R[P a + b] = sum_c W_C^{-ac} [ W_N^{-bc} sum_d W_P^{-bd} (X H / N)[c + C d] ]
+//
+// A block of N complex values (256 KB at N = 32768) is more than a CTA's shared memory but
+// fits one SM's Tensor Memory (128 lanes x 512 columns).  Lane l holds every (b, c) with
+// b mod 128 = l, that is b = l + 128 m, m = 0..31, at complex slot
+// q(c, m) = 32 c + 16 (m & 1) + (m >> 1) (columns 2q and 2q + 1).  Threads t, t + 128,
+// t + 256 and t + 384 of the CTA share lane t mod 128, so every regrouping the split needs
+// stays inside a lane and no data crosses between threads through shared memory outside the
+// P-point transforms themselves:
+//
+//   phase A  thread (s, r) = (t / 128, t mod 128) owns b = r + 128 (8 s + i), i = 0..7.  It
+//            loads xt[blk L - (M-1) + P a + b] for every a (the window was prefetched into L2
+//            while the previous block was being transformed), does the C-point DFTs over a,
+//            multiplies by W_N^{bc} = W_N^{rc} W_{N/128}^{mc} and writes (b, c) to its lane.
+//   phase B  two groups of 256 threads; group g transforms c = g, g + 2, ...  Thread j of a
+//            group holds b = j + 256 e, e = 0..15 (32 contiguous columns of lane j mod 128)
+//            and runs the P-point FFT of fos_fft.cuh (twiddles in shared memory), the
+//            multiply by H[c + C d] / N (stored c-major at plan time), the inverse FFT, and
+//            writes the result back to the same columns.  Meanwhile the next block's input
+//            window is prefetched into L2.
+//   phase C  the ownership of phase A: multiply by W_N^{-bc}; the C-point inverse DFTs over
+//            c give R[P a + b] for every a; R[t] with t >= M - 1 is stored (step 5).
+//
+// Phase A of a thread writes exactly the columns that its phase C read, so phase C of one
+// block and phase A of the next need no barrier between them; two CTA barriers per block
+// order A -> B -> C.  Real input packs two consecutive blocks into one complex transform, as
+// in the other kernels.  Grid: persistent, one CTA per SM (the Tensor Memory allocation),
+// blocks taken round-robin.  The kernel has no waits on other CTAs or on copies.
+#include <type_traits>
+
+#include "fos_fft.cuh"
+#include "fos_kernels.h"
+
+namespace fos {
+
+template <int LOGN, bool REAL>
+struct ResidentCfg {
+    static constexpr int N = 1 << LOGN;
+    static constexpr int LOGP = 12;
+    static constexpr int P = 1 << LOGP;
+    static constexpr int C = N / P;          // 4 or 8
+    static constexpr int HI = N / 128;       // period of W_N^{128 m c} in m c
+    static constexpr int THREADS = 512;
+    static constexpr int GT = 256;           // threads of one phase-B group
+    static constexpr int TM_COLS = 64 * C;   // 32 C complex slots per lane
+    using TL = TwLayout<LOGP, 256>;          // every pass twiddle of the P-point FFT in shared memory
+    static constexpr int BUF = xpad_len(P);  // elements of one exchange buffer
+    // shared memory: 128-byte header (Tensor Memory address), pass twiddles, W_{N/128}^k,
+    // W_N^{rc}, then two exchange buffers per group
+    static constexpr int OFF_TW = 128;
+    static constexpr int OFF_HI = OFF_TW + 8 * TL::SMEM_ENTRIES;
+    static constexpr int OFF_WR = OFF_HI + 8 * HI;
+    static constexpr int OFF_BUF = (OFF_WR + 8 * C * 128 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = OFF_BUF + 2 * 2 * 8 * BUF;
+    static_assert(C == 4 || C == 8, "N = 16384 or 32768");
+    static_assert(TL::SMEM_ENTRIES == FftShape<LOGP>::TW_ENTRIES, "all pass twiddles in shared memory");
+};
+
+// Complex slot pair of steps i0 and i0 + 2 of thread row s: columns of q(c, 8 s + i0) and
+// q(c, 8 s + i0 + 2) = that + 1, relative to c's 64 columns.
+__device__ __forceinline__ uint32_t step_col(int s, int i0) {
+    return 2u * (uint32_t)(16 * (i0 & 1) + 4 * s + (i0 >> 1));
+}
+
+// xt[t] of the first block of the unit (and, for real data, of the second block at t + L):
+// x inside [0, n), S0 in front of it, zeros after it.
+template <bool REAL>
+__device__ __forceinline__ float2 load_point(const BlockParams &p, int64_t t, bool interior) {
+    if constexpr (REAL) {
+        const float *x = static_cast<const float *>(p.x);
+        if (interior) return make_float2(x[t], x[t + p.L]);
+        const float *s0 = static_cast<const float *>(p.state);
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t q = t + (h ? p.L : 0);
+            v[h] = 0.f;
+            if (q >= 0) {
+                if (q < p.n) v[h] = x[q];
+            } else if (q >= -(int64_t)(p.M - 1)) {
+                v[h] = s0[p.M - 1 + q];
+            }
+        }
+        return make_float2(v[0], v[1]);
+    } else {
+        const float2 *x = static_cast<const float2 *>(p.x);
+        if (interior) return x[t];
+        if (t >= 0) return t < p.n ? x[t] : make_float2(0.f, 0.f);
+        if (t >= -(int64_t)(p.M - 1)) return static_cast<const float2 *>(p.state)[p.M - 1 + t];
+        return make_float2(0.f, 0.f);
+    }
+}
+
+// Bulk L2 prefetch of unit u's input window (the part inside x), split over 16 threads.
+template <int LOGN, bool REAL>
+__device__ __forceinline__ void prefetch_window(const BlockParams &p, int64_t u, int tid) {
+    constexpr int SB = REAL ? 4 : 8;
+    constexpr int NPF = 16;
+    if (tid >= NPF) return;
+    const int64_t blk = REAL ? 2 * u : u;
+    int64_t lo = blk * p.L - (p.M - 1);
+    int64_t hi = lo + ResidentCfg<LOGN, REAL>::N + (REAL ? p.L : 0);
+    if (lo < 0) lo = 0;
+    if (hi > p.n) hi = p.n;
+    if (hi <= lo) return;
+    // rounded inwards to 16 bytes, so the range stays inside x
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(p.x);
+    const uintptr_t a0 = (xb + (uintptr_t)lo * SB + 15) & ~uintptr_t(15);
+    const uintptr_t a1 = (xb + (uintptr_t)hi * SB) & ~uintptr_t(15);
+    if (a1 <= a0) return;
+    const uintptr_t piece = ((a1 - a0) / NPF + 15) & ~uintptr_t(15);
+    const uintptr_t b = a0 + (uintptr_t)tid * piece;
+    if (b >= a1) return;
+    const uintptr_t e = b + piece < a1 ? b + piece : a1;
+    prefetch_l2_bulk(reinterpret_cast<const void *>(b), (uint32_t)(e - b));
+}
+
+// Phase A: gather, C-point DFTs over a, twiddle, into this thread's lane.
+template <int LOGN, bool REAL>
+__device__ __forceinline__ void phase_a(const BlockParams &p, int64_t u, uint32_t tlane, int s, int r,
+                                        const float2 *hi_s, const float2 *wr_s) {
+    using R_ = ResidentCfg<LOGN, REAL>;
+    constexpr int C = R_::C, P = R_::P, HI = R_::HI;
+    const int64_t blk = REAL ? 2 * u : u;
+    const int64_t start = blk * p.L - (p.M - 1);
+    const bool interior = start >= 0 && start + R_::N + (REAL ? p.L : 0) <= p.n;
+    float2 wr[C];
+#pragma unroll
+    for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int i0 = (st & 1) + 4 * (st >> 1);  // 0, 1, 4, 5: steps i0 and i0 + 2
+        float2 v[2][C];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int b = r + 128 * (8 * s + i0 + 2 * h);
+#pragma unroll
+            for (int a = 0; a < C; ++a) v[h][a] = load_point<REAL>(p, start + P * a + b, interior);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = 8 * s + i0 + 2 * h;
+            dft<C, -1>(v[h]);
+#pragma unroll
+            for (int c = 1; c < C; ++c) v[h][c] = cmul(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+        }
+        const uint32_t col = step_col(s, i0);
+#pragma unroll
+        for (int c = 0; c < C; ++c) tmem_st4(tlane + 64u * c + col, v[0][c], v[1][c]);
+    }
+    tmem_wait_st();
+}
+
+// Phase B: P-point FFT, multiply by H, inverse FFT for c = g, g + 2, ...
+template <int LOGN, bool REAL>
+__device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
+                                        float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar) {
+    using R_ = ResidentCfg<LOGN, REAL>;
+    constexpr int C = R_::C, P = R_::P;
+    const uint32_t col0 = 32u * (uint32_t)(j >> 7);
+#pragma unroll 1
+    for (int c = g; c < C; c += 2) {
+        const uint32_t ta = tlane + 64u * (uint32_t)c + col0;
+        float2 v[16];
+        {
+            float f0[16], f1[16];
+            tmem_ld16(ta, f0);
+            tmem_ld16(ta + 16u, f1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[e] = make_float2(f0[2 * e], f0[2 * e + 1]);
+                v[8 + e] = make_float2(f1[2 * e], f1[2 * e + 1]);
+            }
+        }
+        fft_tm<R_::LOGP, 256, false>(v, b0, b1, stw, 0u, j, gbar);
+        const float2 *hp = p.H + c * P + j;
+        float2 h[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) h[e] = __ldg(hp + 256 * e);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], h[e]);
+        fft_tm<R_::LOGP, 256, true>(v, b0, b1, stw, 0u, j, gbar);
+        {
+            float f0[16], f1[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                f0[2 * e] = v[e].x;
+                f0[2 * e + 1] = v[e].y;
+                f1[2 * e] = v[8 + e].x;
+                f1[2 * e + 1] = v[8 + e].y;
+            }
+            tmem_st16(ta, f0);
+            tmem_st16(ta + 16u, f1);
+        }
+    }
+    tmem_wait_st();
+}
+
+// Phase C: inverse twiddle, C-point inverse DFTs over c, discard, store.
+template <int LOGN, bool REAL>
+__device__ __forceinline__ void phase_c(const BlockParams &p, int64_t u, uint32_t tlane, int s, int r,
+                                        const float2 *hi_s, const float2 *wr_s) {
+    using R_ = ResidentCfg<LOGN, REAL>;
+    constexpr int C = R_::C, P = R_::P, HI = R_::HI;
+    const int64_t blk = REAL ? 2 * u : u;
+    const int64_t start = blk * p.L - (p.M - 1);  // output index of R[0]
+    const bool whole = start + R_::N + (REAL ? p.L : 0) <= p.n;
+    const int keep = p.M - 1;
+    float2 wr[C];
+#pragma unroll
+    for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const int i0 = (st & 1) + 4 * (st >> 1);
+        const uint32_t col = step_col(s, i0);
+        float2 v[2][C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) tmem_ld4(tlane + 64u * c + col, v[0][c], v[1][c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = 8 * s + i0 + 2 * h;
+#pragma unroll
+            for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+            dft<C, +1>(v[h]);
+            const int b = r + 128 * m;
+#pragma unroll
+            for (int a = 0; a < C; ++a) {
+                const int t = P * a + b;
+                if (t < keep) continue;
+                const int64_t o = start + t;
+                if constexpr (REAL) {
+                    float *y = static_cast<float *>(p.y);
+                    if (whole || o < p.n) st_cs(y + o, v[h][a].x);
+                    if (whole || o + p.L < p.n) st_cs(y + o + p.L, v[h][a].y);
+                } else {
+                    float2 *y = static_cast<float2 *>(p.y);
+                    if (whole || o < p.n) st_cs(y + o, v[h][a]);
+                }
+            }
+        }
+    }
+}
+
+template <int LOGN, bool REAL>
+__global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams p) {
+    using R_ = ResidentCfg<LOGN, REAL>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int s = tid >> 7, r = tid & 127;  // phases A and C
+    const int g = tid >> 8, j = tid & 255;  // phase B
+    uint32_t *tm_slot = reinterpret_cast<uint32_t *>(smem);
+    float2 *stw = reinterpret_cast<float2 *>(smem + R_::OFF_TW);
+    float2 *hi_s = reinterpret_cast<float2 *>(smem + R_::OFF_HI);
+    float2 *wr_s = reinterpret_cast<float2 *>(smem + R_::OFF_WR);
+    float2 *b0 = reinterpret_cast<float2 *>(smem + R_::OFF_BUF) + g * 2 * R_::BUF;
+    float2 *b1 = b0 + R_::BUF;
+    const GroupBarrier<R_::GT> gbar{1 + g};
+
+    int64_t u = blockIdx.x;
+    if (u < p.nunits && !p.no_bulk) prefetch_window<LOGN, REAL>(p, u, tid);
+    if (warp == 0) {
+        tmem_alloc(tm_slot, R_::TM_COLS);
+        tmem_relinquish();
+    }
+    for (int k = tid; k < R_::TL::SMEM_ENTRIES; k += R_::THREADS) stw[k] = p.tw[k];
+    for (int k = tid; k < R_::HI; k += R_::THREADS) hi_s[k] = p.twa[R_::C * 128 + k];
+    for (int k = tid; k < R_::C * 128; k += R_::THREADS) wr_s[k] = p.twa[k];
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tlane = *tm_slot + ((uint32_t)(32 * (warp & 3)) << 16);
+
+    for (; u < p.nunits; u += gridDim.x) {
+        phase_a<LOGN, REAL>(p, u, tlane, s, r, hi_s, wr_s);
+        tmem_fence_before_sync();
+        __syncthreads();  // every (b, c) of the block is in Tensor Memory; S0 has been read
+        tmem_fence_after_sync();
+        if (p.fuse_state && u == 0) {
+            // only unit 0 reads S0 (fuse_state), and n >= M - 1: S0' = the last M-1 samples of x
+            using T_ = typename std::conditional<REAL, float, float2>::type;
+            const T_ *x = static_cast<const T_ *>(p.x);
+            T_ *st = static_cast<T_ *>(p.state);
+            for (int t = tid; t < p.M - 1; t += R_::THREADS) st[t] = x[p.n - (p.M - 1) + t];
+        }
+        const int64_t un = u + gridDim.x;
+        if (un < p.nunits && !p.no_bulk) prefetch_window<LOGN, REAL>(p, un, tid);
+        phase_b<LOGN, REAL>(p, tlane, g, j, b0, b1, stw, gbar);
+        tmem_fence_before_sync();
+        __syncthreads();  // every c has been filtered
+        tmem_fence_after_sync();
+        phase_c<LOGN, REAL>(p, u, tlane, s, r, hi_s, wr_s);
+    }
+
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    if (warp == 0) tmem_dealloc(*tm_slot, R_::TM_COLS);
+}
+
+template <int LOGN, bool REAL>
+KernelEntry resident_entry() {
+    using R_ = ResidentCfg<LOGN, REAL>;
+    KernelEntry k;
+    k.func = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL>);
+    k.threads = R_::THREADS;
+    k.smem = R_::SMEM_BYTES;
+    k.cluster = 1;
+    k.units_per_cta = 1;
+    k.groups = 1;
+    k.fft_logn = R_::LOGP;
+    k.split_c = R_::C;
+    k.state_from_x = 1;
+    return k;
+}
+
+KernelEntry resident_kernel(int logn, bool real) {
+    switch (logn) {
+        case 14: return real ? resident_entry<14, true>() : resident_entry<14, false>();
+        case 15: return real ? resident_entry<15, true>() : resident_entry<15, false>();
+        default: return KernelEntry{};
+    }
+}
+
+}  // namespace fos

@@ -147,7 +147,8 @@ class Plan:
         k, c, g, s = _I(), _I(), _I(), _I()
         _check(lib().fir_os_plan_kernel(self._h, ctypes.byref(k), ctypes.byref(c), ctypes.byref(g),
                                         ctypes.byref(s)))
-        return {"kind": "cluster" if k.value else "cta", "cluster": c.value, "grid": g.value,
+        kind = {0: "cta", 1: "cluster", 2: "tmem-resident"}.get(k.value, str(k.value))
+        return {"kind": kind, "cluster": c.value, "grid": g.value,
                 "smem_bytes": s.value}
 
     def launches(self, n: int) -> int:
