@@ -3,7 +3,7 @@
 //
 // Method: "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法" (zl.czvv.com/42398539.html),
 // 主权项 steps 1-6.  Step 1 (frequency response) runs here at plan time; steps 3-5 run in the
-// fused block kernels (fos_block.cuh, fos_cluster.cu); steps 2 and 6 (moving chunks between
+// fused block kernels (fos_block.cuh, fos_resident.cu, fos_pair.cu); steps 2 and 6 (moving chunks between
 // host and device and repeating) are fir_os_execute_host.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -170,7 +170,7 @@ struct fir_os_plan {
     int device = 0;
     int sms = 0;
     fos::KernelEntry kernel;
-    int max_units_in_flight = 0;  // CTAs (single-CTA kernel) or clusters (cluster kernel)
+    int max_units_in_flight = 0;  // CTAs, or clusters for a cluster kernel
     float2 *d_H = nullptr;
     float2 *d_Hk = nullptr;  // H in the kernel's order, when that is not the natural one
     float2 *d_tw = nullptr;
@@ -408,7 +408,7 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
     if (logn <= 9) p->kernel = fos::block_kernel_small(logn, real);
     else if (logn <= 13) p->kernel = fos::block_kernel_large(logn, real);
     else if (logn <= 15) p->kernel = fos::resident_kernel(logn, real);
-    else p->kernel = fos::cluster_kernel(logn, real);
+    else p->kernel = fos::pair_kernel(logn, real);
     if (!p->kernel.func) return bail(fail(FIR_OS_E_UNSUPPORTED, "no kernel for N = %d", N));
 
     // launch shape
@@ -480,23 +480,6 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
             if ((e = cudaMemcpyAsync(p->d_twa, twa.data(), sizeof(float2) * twa.size(), cudaMemcpyHostToDevice,
                                      stream)) != cudaSuccess)
                 return bail(cuda_fail(e, "split twiddle upload"));
-            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
-        }
-        if (p->kernel.cluster > 1) {
-            const int P = 1 << p->kernel.fft_logn, C = N / P;
-            std::vector<float2> twa((size_t)N);
-            for (int c = 0; c < C; ++c)
-                for (int b = 0; b < P; ++b) {
-                    const long long ex = ((long long)b * c) % N;
-                    const double ang = -2.0 * M_PI * (double)ex / (double)N;
-                    twa[(size_t)c * P + b] = make_float2((float)std::cos(ang), (float)std::sin(ang));
-                }
-            if ((e = cudaMalloc(&p->d_twa, sizeof(float2) * N)) != cudaSuccess)
-                return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(cluster twiddles) failed"));
-            if ((e = cudaMemcpyAsync(p->d_twa, twa.data(), sizeof(float2) * N, cudaMemcpyHostToDevice, stream)) !=
-                cudaSuccess)
-                return bail(cuda_fail(e, "cluster twiddle upload"));
-            // the host vectors must outlive the asynchronous copies
             if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
         }
         if ((e = cudaMemsetAsync(p->d_err, 0, sizeof(int), stream)) != cudaSuccess)

@@ -63,61 +63,9 @@ struct TwLayout {
     static constexpr int TMEM_COLS = tmem_col(S::NPASS);
 };
 
-template <int LOGN, int DIR, int P>
-__device__ __forceinline__ void fft_pass(float2 (&v)[16], float2 *ex, const float2 *__restrict__ tw, int j) {
-    using S = FftShape<LOGN>;
-    if constexpr (P < S::NPASS) {
-        constexpr int T = S::T;
-        constexpr int Ns = S::ns(P);
-        constexpr bool last = (P == S::NPASS - 1);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = ex[xpad(j + e * T)];
-        if constexpr (!last) __syncthreads();  // every read done before the buffer is rewritten
-        const int m = j & (Ns - 1);
-        const float2 *twp = tw + S::twoff(P) + m;
-#pragma unroll
-        for (int r = 1; r < 16; ++r) v[r] = ctw<DIR>(v[r], __ldg(twp + (r - 1) * Ns));
-        dft<16, DIR>(v);
-        if constexpr (!last) {
-            const int base = (j / Ns) * (16 * Ns) + m;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) ex[xpad(base + r * Ns)] = v[r];
-            __syncthreads();
-        }
-        fft_pass<LOGN, DIR, P + 1>(v, ex, tw, j);
-    }
-}
-
-// Transform v in place (layout above).  `ex` is this transform's N-element exchange buffer.
-// sync_first: the buffer may still be read by other threads of the CTA (a previous transform),
-// so barrier before the first write.
-template <int LOGN, int DIR>
-__device__ __forceinline__ void fft_regs(float2 (&v)[16], float2 *ex, const float2 *__restrict__ tw, int j,
-                                         bool sync_first) {
-    using S = FftShape<LOGN>;
-    constexpr int T = S::T, R0 = S::R0, G = 16 / R0;
-    // pass 0: radix R0 on groups g = j + q T; element r of group g is z[g + r N/R0] = v[q + r G]
-#pragma unroll
-    for (int q = 0; q < G; ++q) {
-        float2 a[R0];
-#pragma unroll
-        for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
-        dft<R0, DIR>(a);
-#pragma unroll
-        for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
-    }
-    if (sync_first) __syncthreads();
-#pragma unroll
-    for (int q = 0; q < G; ++q)
-#pragma unroll
-        for (int r = 0; r < R0; ++r) ex[xpad((j + q * T) * R0 + r)] = v[q + r * G];
-    __syncthreads();
-    fft_pass<LOGN, DIR, 1>(v, ex, tw, j);
-}
-
 // ---------------------------------------------------------------------------------------
-// Variant with per-thread twiddles in Tensor Memory (or, for passes with Ns <= SMAX, in the
-// shared table `stw`), laid out as TwLayout<LOGN, SMAX> describes.  The passes alternate between two
+// The transform, with per-thread twiddles in Tensor Memory (or, for passes with Ns <= SMAX, in
+// the shared table `stw`), laid out as TwLayout<LOGN, SMAX> describes.  The passes alternate between two
 // exchange buffers, so each pass needs one barrier: pass p of the forward transform
 // (INV = false) writes buffer (p mod 2) and reads buffer ((p-1) mod 2); the inverse transform
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward

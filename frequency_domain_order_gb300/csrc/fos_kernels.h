@@ -14,8 +14,8 @@ struct BlockParams {
     const float2 *H;       // N bins, H / N: natural order, or c-major (H[c + C d] at [c P + d])
                            // for the resident kernel
     const float2 *tw;      // Stockham pass twiddles of the per-CTA transform
-    const float2 *twa;     // cluster kernel: W_N^{b c} at [c * P + b]; resident kernel:
-                           // W_N^{r c} at [c * 128 + r], then W_N^{128 k} at [C * 128 + k]
+    const float2 *twa;     // resident / pair kernels: W_N^{r c} at [c * 128 + r] (c < C),
+                           // then W_N^{128 k} at [C * 128 + k] (k < N / 128)
     int *err;              // device error word (set to 1 when a bounded wait ran out)
     int64_t n;             // samples in this call
     int64_t nunits;        // work units (block groups / blocks / block pairs)
@@ -40,10 +40,10 @@ struct KernelEntry {
 // Single-CTA kernels, N = 2^logn, logn in [6, 13].
 KernelEntry block_kernel_small(int logn, bool real);   // logn 6..9
 KernelEntry block_kernel_large(int logn, bool real);   // logn 10..13
-// Cluster kernels, N = 2^logn, logn in [14, 16].
-KernelEntry cluster_kernel(int logn, bool real);
 // One block resident in one SM's Tensor Memory, N = 2^logn, logn in [14, 15].
 KernelEntry resident_kernel(int logn, bool real);
+// One block in the Tensor Memory of a two-CTA cluster, N = 2^16.
+KernelEntry pair_kernel(int logn, bool real);
 
 // Entries of the pass-twiddle table for a per-CTA transform of 2^logn points.
 int pass_twiddle_entries(int logn);

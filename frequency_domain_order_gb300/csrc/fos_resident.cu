@@ -36,8 +36,7 @@
 // blocks taken round-robin.  The kernel has no waits on other CTAs or on copies.
 #include <type_traits>
 
-#include "fos_fft.cuh"
-#include "fos_kernels.h"
+#include "fos_resident.cuh"
 
 namespace fos {
 
@@ -63,65 +62,6 @@ struct ResidentCfg {
     static_assert(C == 4 || C == 8, "N = 16384 or 32768");
     static_assert(TL::SMEM_ENTRIES == FftShape<LOGP>::TW_ENTRIES, "all pass twiddles in shared memory");
 };
-
-// Complex slot pair of steps i0 and i0 + 2 of thread row s: columns of q(c, 8 s + i0) and
-// q(c, 8 s + i0 + 2) = that + 1, relative to c's 64 columns.
-__device__ __forceinline__ uint32_t step_col(int s, int i0) {
-    return 2u * (uint32_t)(16 * (i0 & 1) + 4 * s + (i0 >> 1));
-}
-
-// xt[t] of the first block of the unit (and, for real data, of the second block at t + L):
-// x inside [0, n), S0 in front of it, zeros after it.
-template <bool REAL>
-__device__ __forceinline__ float2 load_point(const BlockParams &p, int64_t t, bool interior) {
-    if constexpr (REAL) {
-        const float *x = static_cast<const float *>(p.x);
-        if (interior) return make_float2(x[t], x[t + p.L]);
-        const float *s0 = static_cast<const float *>(p.state);
-        float v[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t q = t + (h ? p.L : 0);
-            v[h] = 0.f;
-            if (q >= 0) {
-                if (q < p.n) v[h] = x[q];
-            } else if (q >= -(int64_t)(p.M - 1)) {
-                v[h] = s0[p.M - 1 + q];
-            }
-        }
-        return make_float2(v[0], v[1]);
-    } else {
-        const float2 *x = static_cast<const float2 *>(p.x);
-        if (interior) return x[t];
-        if (t >= 0) return t < p.n ? x[t] : make_float2(0.f, 0.f);
-        if (t >= -(int64_t)(p.M - 1)) return static_cast<const float2 *>(p.state)[p.M - 1 + t];
-        return make_float2(0.f, 0.f);
-    }
-}
-
-// Bulk L2 prefetch of unit u's input window (the part inside x), split over 16 threads.
-template <int LOGN, bool REAL>
-__device__ __forceinline__ void prefetch_window(const BlockParams &p, int64_t u, int tid) {
-    constexpr int SB = REAL ? 4 : 8;
-    constexpr int NPF = 16;
-    if (tid >= NPF) return;
-    const int64_t blk = REAL ? 2 * u : u;
-    int64_t lo = blk * p.L - (p.M - 1);
-    int64_t hi = lo + ResidentCfg<LOGN, REAL>::N + (REAL ? p.L : 0);
-    if (lo < 0) lo = 0;
-    if (hi > p.n) hi = p.n;
-    if (hi <= lo) return;
-    // rounded inwards to 16 bytes, so the range stays inside x
-    const uintptr_t xb = reinterpret_cast<uintptr_t>(p.x);
-    const uintptr_t a0 = (xb + (uintptr_t)lo * SB + 15) & ~uintptr_t(15);
-    const uintptr_t a1 = (xb + (uintptr_t)hi * SB) & ~uintptr_t(15);
-    if (a1 <= a0) return;
-    const uintptr_t piece = ((a1 - a0) / NPF + 15) & ~uintptr_t(15);
-    const uintptr_t b = a0 + (uintptr_t)tid * piece;
-    if (b >= a1) return;
-    const uintptr_t e = b + piece < a1 ? b + piece : a1;
-    prefetch_l2_bulk(reinterpret_cast<const void *>(b), (uint32_t)(e - b));
-}
 
 // Phase A: gather, C-point DFTs over a, twiddle, into this thread's lane.
 template <int LOGN, bool REAL>
@@ -155,52 +95,6 @@ __device__ __forceinline__ void phase_a(const BlockParams &p, int64_t u, uint32_
         const uint32_t col = step_col(s, i0);
 #pragma unroll
         for (int c = 0; c < C; ++c) tmem_st4(tlane + 64u * c + col, v[0][c], v[1][c]);
-    }
-    tmem_wait_st();
-}
-
-// Phase B: P-point FFT, multiply by H, inverse FFT for c = g, g + 2, ...
-template <int LOGN, bool REAL>
-__device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
-                                        float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar) {
-    using R_ = ResidentCfg<LOGN, REAL>;
-    constexpr int C = R_::C, P = R_::P;
-    const uint32_t col0 = 32u * (uint32_t)(j >> 7);
-#pragma unroll 1
-    for (int c = g; c < C; c += 2) {
-        const uint32_t ta = tlane + 64u * (uint32_t)c + col0;
-        float2 v[16];
-        {
-            float f0[16], f1[16];
-            tmem_ld16(ta, f0);
-            tmem_ld16(ta + 16u, f1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                v[e] = make_float2(f0[2 * e], f0[2 * e + 1]);
-                v[8 + e] = make_float2(f1[2 * e], f1[2 * e + 1]);
-            }
-        }
-        fft_tm<R_::LOGP, 256, false>(v, b0, b1, stw, 0u, j, gbar);
-        const float2 *hp = p.H + c * P + j;
-        float2 h[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) h[e] = __ldg(hp + 256 * e);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], h[e]);
-        fft_tm<R_::LOGP, 256, true>(v, b0, b1, stw, 0u, j, gbar);
-        {
-            float f0[16], f1[16];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                f0[2 * e] = v[e].x;
-                f0[2 * e + 1] = v[e].y;
-                f1[2 * e] = v[8 + e].x;
-                f1[2 * e + 1] = v[8 + e].y;
-            }
-            tmem_st16(ta, f0);
-            tmem_st16(ta + 16u, f1);
-        }
     }
     tmem_wait_st();
 }
@@ -268,7 +162,7 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     const GroupBarrier<R_::GT> gbar{1 + g};
 
     int64_t u = blockIdx.x;
-    if (u < p.nunits && !p.no_bulk) prefetch_window<LOGN, REAL>(p, u, tid);
+    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, u, tid);
     if (warp == 0) {
         tmem_alloc(tm_slot, R_::TM_COLS);
         tmem_relinquish();
@@ -294,8 +188,8 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
             for (int t = tid; t < p.M - 1; t += R_::THREADS) st[t] = x[p.n - (p.M - 1) + t];
         }
         const int64_t un = u + gridDim.x;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<LOGN, REAL>(p, un, tid);
-        phase_b<LOGN, REAL>(p, tlane, g, j, b0, b1, stw, gbar);
+        if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, un, tid);
+        phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1);
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();

@@ -133,8 +133,9 @@ int fir_os_plan_destroy(fir_os_plan_t plan);
 int fir_os_plan_info(fir_os_plan_t plan, int *M, int *N, int *L);
 
 /* fir_os_plan_kernel -- which block kernel a plan launches: 0 = one CTA per block group
- * (N <= 8192), 1 = a thread-block cluster per block (N = 65536), 2 = one block resident in
- * one SM's Tensor Memory (N = 16384, 32768).  *cluster_size is 1 or
+ * (N <= 8192), 1 = a two-CTA cluster per block, half of it in each SM's Tensor Memory
+ * (N = 65536), 2 = one block resident in one SM's Tensor Memory (N = 16384, 32768).
+ * *cluster_size is 1 or
  * the cluster's CTA count; *grid the CTAs one launch uses; *smem_bytes the dynamic shared
  * memory per CTA.  Any output pointer may be NULL. */
 int fir_os_plan_kernel(fir_os_plan_t plan, int *kind, int *cluster_size, int *grid,
