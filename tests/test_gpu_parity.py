@@ -77,6 +77,36 @@ def test_scaled_workload(name, blocks, tail, calls):
     assert np.array_equal(st, x[-(w.M - 1):])
 
 
+# ----------------------------------------------------------------------------- shards
+
+
+@pytest.mark.parametrize("name,blocks,tail,parts", [
+    ("C2", 37, 1001, 4), ("C3", 9, 12345, 3), ("C4", 41, 123, 5), ("C5", 5, 777, 2),
+])
+def test_shards_with_halos_equal_one_call(name, blocks, tail, parts):
+    """Each shard filtered by its own call, its halo (the M-1 samples before it) as the state:
+    the outputs concatenate to one call's bit for bit, and the last shard's state is S0'."""
+    from frequency_domain_order_gb300.shard import shard_ranges, shard_states
+    torch = pytest.importorskip("torch")
+    w = W.scaled(W.WORKLOADS[name], blocks, tail)
+    x = W.make_x(w)
+    s0 = W.make_x(W.scaled(w, 1))[: w.M - 1]
+    plan = make_plan(w)
+    xd = to_dev(x)
+    y1, st1 = run_device(plan, xd, (w.n,), to_dev(s0))
+    ranges = shard_ranges(w.n, w.L, parts, real=w.real)
+    states = shard_states(xd, to_dev(s0), ranges, w.M)
+    y2 = torch.empty_like(xd)
+    for (a, b), st in zip(ranges, states):
+        st = st.clone()
+        plan.execute(xd[a:b], y2[a:b], st)
+        last = st
+    torch.cuda.synchronize()
+    plan.device_status()
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+    assert np.array_equal(st1.cpu().numpy(), last.cpu().numpy())
+
+
 # ----------------------------------------------------------------------------- full size, sampled
 
 

@@ -220,6 +220,17 @@ def make_x(w: Workload) -> np.ndarray:
     return complex_normal(w.n, w.x_seed).astype(np.complex64)
 
 
+def make_x_shard(w: Workload, g: int) -> np.ndarray:
+    """Shard g of a stream of several workload-sized shards (one per GPU of a multi-GPU run):
+    shard 0 is make_x(w); shard g > 0 draws the same distribution from seed x_seed + 1000 g."""
+    if g == 0:
+        return make_x(w)
+    seed = w.x_seed + 1000 * g
+    if w.real:
+        return uniform_real(w.n, seed).astype(np.float32)
+    return complex_normal(w.n, seed).astype(np.complex64)
+
+
 def make_state0(w: Workload) -> np.ndarray:
     """Initial state S0 = 0 (M-1 samples)."""
     return np.zeros(w.M - 1, dtype=np.float32 if w.real else np.complex64)
