@@ -67,11 +67,15 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback", {}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
+    """Hash of the named kernel sources (file names under the package's csrc/)."""
     csrc = os.path.join(ROOT, "frequency_domain_order_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for name in sorted(files):
+        path = os.path.join(csrc, name)
+        if not os.path.exists(path):
+            return "missing:" + name
+        with open(path, "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -79,13 +83,13 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic(config: str):
     """dram bytes per launch from a committed ncu summary for this workload, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel (the files the summary lists); else None."""
     p = os.path.join(PROFILE_DIR, f"traffic_{config}.json")
     if not os.path.exists(p):
         return None, None
     with open(p) as f:
         d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
+    if d.get("source_hash") != kernel_source_hash(d.get("source_files", [])):
         return None, d.get("source_hash")
     return float(d["dram_bytes_per_launch"]), d.get("source_hash")
 

@@ -287,25 +287,29 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     const int64_t want = (bp.nunits + p->kernel.groups - 1) / p->kernel.groups;
     const int64_t groups = want < p->max_units_in_flight ? want : p->max_units_in_flight;
     void *args[] = {&bp};
-    if (p->kernel.cluster == 1) {
-        FOS_CUDA(cudaLaunchKernel(p->kernel.func, dim3((unsigned)groups), dim3(p->kernel.threads), args,
-                                  (size_t)p->kernel.smem, stream),
-                 "block kernel launch");
-    } else {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3((unsigned)(groups * p->kernel.cluster));
-        cfg.blockDim = dim3(p->kernel.threads);
-        cfg.dynamicSmemBytes = (size_t)p->kernel.smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p->kernel.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        FOS_CUDA(cudaLaunchKernelExC(&cfg, p->kernel.func, args), "cluster kernel launch");
+    // programmatic serialization: the kernel's set-up (Tensor Memory, plan constants) overlaps
+    // the end of the kernel before it in the stream; it waits for that kernel before it touches
+    // x, y or the state
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(groups * p->kernel.cluster));
+    cfg.blockDim = dim3(p->kernel.threads);
+    cfg.dynamicSmemBytes = (size_t)p->kernel.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p->kernel.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p->kernel.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    FOS_CUDA(cudaLaunchKernelExC(&cfg, p->kernel.func, args), "block kernel launch");
     if (!bp.fuse_state && p->M > 1) {
         if (real)
             fos_state_kernel<float><<<1, 1024, 0, stream>>>(static_cast<const float *>(x), n,

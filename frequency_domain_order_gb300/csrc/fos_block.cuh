@@ -25,11 +25,13 @@
 // the second exchange buffer once it has been read.
 //
 // A CTA that allocates Tensor Memory runs alone on its SM, so a CTA has 512 threads split
-// into independent groups (two groups of 256 for N <= 4096, one of 512 for N = 8192), each
-// with its own three buffers, mbarriers and hardware barrier, sharing only the Tensor Memory
-// allocation.  Grid: persistent, one CTA per SM; the groups of all CTAs take work units
-// round-robin.  A work unit is F consecutive blocks (complex) or F consecutive block pairs
-// (real), F = max(1, 256 / (N/16)), each handled by N/16 threads.
+// into independent groups of max(64, N/16) threads (eight groups for N <= 1024, two for
+// N = 4096, one for N = 8192), each with its own three buffers, mbarriers and hardware barrier,
+// sharing only the Tensor Memory allocation.  Grid: persistent, one CTA per SM; the groups of
+// all CTAs take work units round-robin.  A work unit is F consecutive blocks (complex) or F
+// consecutive block pairs (real), F = max(1, 64 / (N/16)), each handled by N/16 threads: small
+// transforms spread over as many groups as possible, so that a call of few blocks finishes in
+// the time of one unit.
 #pragma once
 
 #include <type_traits>
@@ -44,9 +46,9 @@ struct BlockCfg {
     using S = FftShape<LOGN>;
     static constexpr int N = S::N;
     static constexpr int T = S::T;
-    static constexpr int F = T >= 256 ? 1 : 256 / T;
-    static constexpr int GT = F * T;              // threads of one group (256, or 512 for N = 8192)
-    static constexpr int GROUPS = 512 / GT;       // independent groups per CTA
+    static constexpr int F = T >= 64 ? 1 : 64 / T;
+    static constexpr int GT = F * T;              // threads of one group: max(64, N / 16)
+    static constexpr int GROUPS = 512 / GT;       // independent groups per CTA (8 .. 1)
     static constexpr int THREADS = 512;
     static constexpr int SB = REAL ? 4 : 8;  // bytes per sample
     // F blocks' gather windows (complex: (F-1)L + N samples; real: (2F-1)L + N floats) fit in
@@ -54,7 +56,10 @@ struct BlockCfg {
     // The same buffer then serves as the F padded exchange buffers (8 F xpad_len(N) bytes).
     static constexpr int EX_BYTES = 8 * F * xpad_len(N);
     static constexpr int BUF_BYTES = (((8 * F * N + 32) > EX_BYTES ? (8 * F * N + 32) : EX_BYTES) + 127) / 128 * 128;
-    static constexpr int SMEM_BYTES = 128 + GROUPS * 3 * BUF_BYTES;
+    static constexpr int HDR_BYTES = 256;  // Tensor Memory address at 0, group g's mbarriers at 16 + 16 g
+    static constexpr int SMEM_BYTES = HDR_BYTES + GROUPS * 3 * BUF_BYTES;
+    static_assert(16 + 16 * GROUPS <= HDR_BYTES, "header");
+    static_assert(GROUPS <= 15, "one hardware barrier id per group");
     static constexpr int MIN_BLOCKS = 1;  // a CTA that allocates Tensor Memory runs alone on its SM
     // Tensor Memory: per thread 32 columns of H bins + 32 per twiddled pass; warps w, w+4, ...
     // share a lane range and take consecutive column ranges.
@@ -164,14 +169,15 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     const int tg = tid % C::GT;     // thread within the group
     const int f = tg / T;           // transform slot within the group
     const int j = tg % T;           // thread within the transform
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + 2 * g;
-    uint32_t *tm_base_slot = reinterpret_cast<uint32_t *>(smem + 64);
-    unsigned char *gbase = smem + 128 + g * 3 * C::BUF_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 16) + 2 * g;
+    uint32_t *tm_base_slot = reinterpret_cast<uint32_t *>(smem);
+    unsigned char *gbase = smem + C::HDR_BYTES + g * 3 * C::BUF_BYTES;
     float2 *xbuf = reinterpret_cast<float2 *>(gbase);  // exchange buffer
     unsigned char *stg0 = gbase + C::BUF_BYTES;
     unsigned char *stg1 = gbase + 2 * C::BUF_BYTES;
     const typename C::Bar gbar{1 + g};
 
+    griddep_launch_dependents();  // the next call's kernel may start its own set-up
     if (warp == 0) {
         tmem_alloc(tm_base_slot, C::TM_COLS);
         tmem_relinquish();
@@ -192,11 +198,9 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     int ocur = 0, onxt = 0;           // element offset of the window in the buffer
     bool allow_tma = !p.no_bulk;  // bulk copies read device memory only
 
-    // the groups of all CTAs take work units round-robin; the first unit's copy is started
-    // before the Tensor Memory set-up so that the two latencies overlap
+    // the groups of all CTAs take work units round-robin
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
     int64_t u = (int64_t)blockIdx.x * C::GROUPS + g;
-    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur, tg, gbar);
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
     const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
@@ -235,6 +239,11 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
             }
         tmem_wait_st();
     }
+
+    // everything above reads plan memory only; x, y and the state may belong to the kernel
+    // before this one in the stream, which has to be complete from here on
+    griddep_wait();
+    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur, tg, gbar);
 
     // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
     const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;

@@ -245,6 +245,15 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the stream (when
+// it was launched with programmatic serialization) start on free SMs; wait returns once the
+// kernel before this one has completed and its memory operations are visible.  A kernel
+// touches nothing that an earlier kernel of the stream may write before it has waited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // streaming (evict-first) global stores
 __device__ __forceinline__ void st_cs(float2 *p, float2 v) { __stcs(p, v); }
 __device__ __forceinline__ void st_cs(float *p, float v) { __stcs(p, v); }

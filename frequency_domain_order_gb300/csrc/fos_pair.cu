@@ -218,9 +218,10 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     const uint32_t peer_recv = map_rank(smem_addr(bufs), kappa ^ 1u);
     const GroupBarrier<256> gbar{1 + g};
 
+    griddep_launch_dependents();  // the next call's kernel may start its own set-up
     int64_t u = cluster_id_x();
     const int64_t ncl = nclusters_x();
-    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, u, tid, (int)kappa, 2);
+    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, u, tid, (int)kappa, 2);  // a hint
     if (warp == 0) {
         tmem_alloc(tm_slot, Q::TM_COLS);
         tmem_relinquish();
@@ -232,6 +233,8 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     cluster_sync();  // both CTAs are running (and set up) before any remote store
     tmem_fence_after_sync();
     const uint32_t tlane = *tm_slot + ((uint32_t)(32 * (warp & 3)) << 16);
+    // the set-up read plan memory only; x, y and the state may belong to the previous kernel
+    griddep_wait();
 
     for (; u < p.nunits; u += ncl) {
         pair_phase_a<REAL>(p, u, kappa, tlane, s, r, hi_s, wr_s);

@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     float2 *b1 = b0 + R_::BUF;
     const GroupBarrier<R_::GT> gbar{1 + g};
 
+    griddep_launch_dependents();  // the next call's kernel may start its own set-up
     int64_t u = blockIdx.x;
-    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, u, tid);
+    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, u, tid);  // a hint only
     if (warp == 0) {
         tmem_alloc(tm_slot, R_::TM_COLS);
         tmem_relinquish();
@@ -174,6 +175,8 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tlane = *tm_slot + ((uint32_t)(32 * (warp & 3)) << 16);
+    // the set-up read plan memory only; x, y and the state may belong to the previous kernel
+    griddep_wait();
 
     for (; u < p.nunits; u += gridDim.x) {
         phase_a<LOGN, REAL>(p, u, tlane, s, r, hi_s, wr_s);
