@@ -212,7 +212,8 @@ def config_block(w: W.Workload, footprint: int):
         "host CPU run (no GPU L2 involved)"
     return {
         "workload": f"{w.name}: {w.description}",
-        "n_samples": w.n, "calls_per_step": len(w.calls), "M": w.M, "N": w.N, "L": w.L,
+        "n_samples": w.n * w.channels, "channels": w.channels, "calls_per_step": len(w.calls),
+        "M": w.M, "N": w.N, "L": w.L,
         "sample": "float32" if w.real else "complex64",
         "coefficients": "H given (complex64)" if w.coef == "freq" else "h taps",
         "l2": l2,
@@ -234,11 +235,17 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
         fbuild.build()
     barrier(world)
 
-    # rank g filters shard g of one stream of `world` workload-sized shards; its state starts
-    # as the halo: the last M-1 samples of shard g-1 (zeros for shard 0)
-    x = W.make_x_shard(w, rank)
-    halo = (W.make_x_shard(w, rank - 1)[w.n - (w.M - 1):] if rank > 0
-            else W.make_state0(w))
+    if w.channels == 1:
+        # rank g filters shard g of one stream of `world` workload-sized shards; its state
+        # starts as the halo: the last M-1 samples of shard g-1 (zeros for shard 0)
+        x = W.make_x_shard(w, rank)
+        halo = (W.make_x_shard(w, rank - 1)[w.n - (w.M - 1):] if rank > 0
+                else W.make_state0(w))
+    else:
+        # a bank of channels: rank g filters channels g C .. g C + C - 1 of a world-wide bank
+        # (independent streams, each from a zero state)
+        x = np.stack([W.make_x_shard(w, rank * w.channels + c) for c in range(w.channels)])
+        halo = np.zeros((w.channels, w.M - 1), dtype=x.dtype)
     if w.coef == "freq":
         coef = torch.from_numpy(W.make_H_given(w)).to(dev)
         plan = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=fir_os.COEF_FREQ)
@@ -252,22 +259,29 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     footprint = sets * 2 * x.nbytes
     stream = torch.cuda.current_stream(dev)
 
+    def call(k, off, c, strm):
+        if w.channels == 1:
+            plan.execute(xs[k][off: off + c], ys[k][off: off + c], sts[k], strm)
+        else:
+            plan.execute_batched(xs[k][:, off: off + c], ys[k][:, off: off + c], sts[k], strm)
+
     def step(i, evs=None):
         k = i % sets
         off = 0
         for q, c in enumerate(w.calls):
             if evs is not None:
                 evs[q][0].record(stream)
-            plan.execute(xs[k][off: off + c], ys[k][off: off + c], sts[k], stream)
+            call(k, off, c, stream)
             if evs is not None:
                 evs[q][1].record(stream)
             off += c
 
     ncall = len(w.calls)
     graphs = None
-    if ncall > 1:
-        # a step of many small calls is launch-bound from Python: capture each buffer set's
-        # calls once into a CUDA graph and replay it (the calls are plain kernel launches)
+    if not args.direct:
+        # capture each buffer set's calls once into a CUDA graph and replay it: a step of small
+        # calls is otherwise bound by the Python launch path, and an event pair around a direct
+        # launch includes the host's launch latency (the calls are plain kernel launches)
         step(0)
         step(1)
         torch.cuda.synchronize()
@@ -278,7 +292,7 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
                 cap = torch.cuda.current_stream(dev)
                 off = 0
                 for c in w.calls:
-                    plan.execute(xs[k][off: off + c], ys[k][off: off + c], sts[k], cap)
+                    call(k, off, c, cap)
                     off += c
             graphs.append(g)
 
@@ -318,9 +332,10 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     ms_step = reduce_max(total_ms / K, world, dev)
     launches_per_step = sum(plan.launches(c) for c in w.calls)
 
-    value = world * w.n / (ms_step * 1e-3) / 1e9
+    total = w.n * w.channels  # output samples of one step on one GPU
+    value = world * total / (ms_step * 1e-3) / 1e9
     peak, peak_kind, peaks = measured_peaks()
-    bytes_step = w.n * bytes_per_output(w)
+    bytes_step = total * bytes_per_output(w)
     bytes_launch = bytes_step / ncall
     achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
     traffic, _ = profiled_traffic(w.name)
@@ -328,20 +343,23 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     sm_mhz = clk["sm_mhz"] if clk else (peaks.get("sm_max_mhz") or 2070.0)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
-    flops_step = w.n * flops_per_output(w)
+    flops_step = total * flops_per_output(w)
     t_hbm = bytes_step / (peak * 1e9)
     t_fp32 = flops_step / (fp32_peak * 1e12)
 
     # end to end through the host-buffer entry point (pinned memory, copies in the timed region)
+    # (a bank of channels: one host-buffer call per channel)
     xh = torch.from_numpy(x).pin_memory()
     yh = torch.empty_like(xh).pin_memory()
-    sh = torch.zeros(w.M - 1, dtype=xh.dtype).pin_memory()
+    sh = torch.zeros((w.channels, w.M - 1) if w.channels > 1 else (w.M - 1,), dtype=xh.dtype).pin_memory()
 
     def e2e_step():
-        off = 0
-        for c in w.calls:
-            plan.execute_host(xh[off: off + c], yh[off: off + c], sh, stream)
-            off += c
+        for ch in range(w.channels):
+            xr, yr, sr = (xh[ch], yh[ch], sh[ch]) if w.channels > 1 else (xh, yh, sh)
+            off = 0
+            for c in w.calls:
+                plan.execute_host(xr[off: off + c], yr[off: off + c], sr, stream)
+                off += c
 
     for _ in range(max(1, min(args.warmup, 3))):
         e2e_step()
@@ -353,9 +371,9 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     torch.cuda.synchronize()
     e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, world, dev)
     sb = w.sample_bytes
-    e2e = {"value": world * w.n / e2e_s / 1e9, "unit": "GS/s",
-           "h2d_bytes_per_step": w.n * sb + len(w.calls) * (w.M - 1) * sb,
-           "d2h_bytes_per_step": w.n * sb + len(w.calls) * (w.M - 1) * sb,
+    e2e = {"value": world * total / e2e_s / 1e9, "unit": "GS/s",
+           "h2d_bytes_per_step": w.channels * (w.n * sb + len(w.calls) * (w.M - 1) * sb),
+           "d2h_bytes_per_step": w.channels * (w.n * sb + len(w.calls) * (w.M - 1) * sb),
            "steps": e2e_steps,
            "path": "fir_os_execute_host on page-locked host buffers: the fused kernel reads x and "
                    "writes y and the state in host memory in place over the host link"}
@@ -391,7 +409,8 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
         "wall_s_timed_region": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+        # (a bank of channels: the oracle on channel 0, the same per-sample work)
+        out["cpu_baseline"] = cpu_baseline(w, x if w.channels == 1 else x[0], budget_s=args.cpu_budget)
     plan.close()
     return out
 
@@ -470,6 +489,8 @@ def main(argv=None):
     ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--direct", action="store_true",
+                    help="launch each call from Python (per-launch events) instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

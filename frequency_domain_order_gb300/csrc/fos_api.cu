@@ -104,8 +104,11 @@ __global__ void fos_permute_h(const float2 *H, float2 *Hk, int N, int C) {
 // cannot write the state itself (more than one work unit reads S0).  For n < M-1 the kept
 // part of S0 moves towards the front; chunks are read completely before they are written and
 // every later chunk reads only indices beyond what earlier chunks wrote.
+// One CTA per channel: channel c's x and state start at c * x_stride and c * s_stride.
 template <typename T>
-__global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist) {
+__global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist, int64_t x_stride, int64_t s_stride) {
+    x += blockIdx.x * x_stride;
+    state += blockIdx.x * s_stride;
     if (n >= hist) {
         for (int t = threadIdx.x; t < hist; t += blockDim.x) state[t] = x[n - hist + t];
         return;
@@ -266,8 +269,11 @@ bool fuse_state(const fir_os_plan *p, int64_t n) {
     return span >= p->M - 1 && n >= p->M - 1;
 }
 
+// One call over `channels` streams of n samples each; channel c's x, y and state start at
+// c * xs, c * ys and c * ss samples.
 int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state, cudaStream_t stream,
-                  bool host_resident = false) {
+                  bool host_resident = false, int channels = 1, int64_t xs = 0, int64_t ys = 0,
+                  int64_t ss = 0) {
     const bool real = p->data_kind == FIR_OS_REAL;
     fos::BlockParams bp{};
     bp.x = x;
@@ -278,7 +284,11 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.twa = p->d_twa;
     bp.err = p->d_err;
     bp.n = n;
-    bp.nunits = units_for(p, n);
+    bp.upc = units_for(p, n);
+    bp.nunits = bp.upc * channels;
+    bp.x_stride = xs;
+    bp.y_stride = ys;
+    bp.s_stride = ss;
     bp.M = p->M;
     bp.L = p->L;
     bp.fuse_state = fuse_state(p, n);
@@ -312,11 +322,11 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     FOS_CUDA(cudaLaunchKernelExC(&cfg, p->kernel.func, args), "block kernel launch");
     if (!bp.fuse_state && p->M > 1) {
         if (real)
-            fos_state_kernel<float><<<1, 1024, 0, stream>>>(static_cast<const float *>(x), n,
-                                                            static_cast<float *>(state), p->M - 1);
+            fos_state_kernel<float><<<channels, 1024, 0, stream>>>(static_cast<const float *>(x), n,
+                                                                   static_cast<float *>(state), p->M - 1, xs, ss);
         else
-            fos_state_kernel<float2><<<1, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
-                                                             static_cast<float2 *>(state), p->M - 1);
+            fos_state_kernel<float2><<<channels, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
+                                                                    static_cast<float2 *>(state), p->M - 1, xs, ss);
         FOS_CUDA(cudaGetLastError(), "state kernel launch");
     }
     return FIR_OS_OK;
@@ -592,6 +602,35 @@ int fir_os_execute(fir_os_plan_t plan, const void *x, int64_t n, void *y, void *
     int rc = check_device(plan);
     if (rc) return rc;
     return launch_blocks(plan, x, n, y, state, static_cast<cudaStream_t>(stream_));
+}
+
+int fir_os_execute_batched(fir_os_plan_t plan, const void *x, int64_t x_stride, void *y, int64_t y_stride,
+                           void *state, int64_t state_stride, int64_t n, int channels, void *stream_) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (n < 0) return fail(FIR_OS_E_INVAL, "n_samples < 0");
+    if (channels < 1) return fail(FIR_OS_E_INVAL, "channels must be >= 1");
+    if (n == 0) return FIR_OS_OK;
+    const int sb = sample_bytes(plan);
+    const int hist = plan->M - 1;
+    if (!x || !y) return fail(FIR_OS_E_INVAL, "x or y is NULL");
+    if (hist > 0 && !state) return fail(FIR_OS_E_INVAL, "state is NULL but M > 1");
+    if (channels > 1 && (x_stride < n || y_stride < n || (hist > 0 && state_stride < hist)))
+        return fail(FIR_OS_E_INVAL, "strides must be at least n_samples (x, y) and M-1 (state)");
+    if (x_stride < 0 || y_stride < 0 || state_stride < 0) return fail(FIR_OS_E_INVAL, "negative stride");
+    const uintptr_t ux = reinterpret_cast<uintptr_t>(x), uy = reinterpret_cast<uintptr_t>(y),
+                    us = reinterpret_cast<uintptr_t>(state);
+    if ((ux | uy) & (uintptr_t)(sb - 1) || (hist > 0 && (us & (uintptr_t)(sb - 1))))
+        return fail(FIR_OS_E_ALIGN, "x, y and state must be %d-byte aligned", sb);
+    // the whole extents (first to last channel) of x, y and the state must be disjoint
+    const size_t xe = ((size_t)(channels - 1) * x_stride + n) * sb, ye = ((size_t)(channels - 1) * y_stride + n) * sb;
+    const size_t se = hist > 0 ? ((size_t)(channels - 1) * state_stride + hist) * sb : 0;
+    if (ranges_overlap(ux, xe, uy, ye)) return fail(FIR_OS_E_INVAL, "x and y overlap");
+    if (ranges_overlap(us, se, ux, xe) || ranges_overlap(us, se, uy, ye))
+        return fail(FIR_OS_E_INVAL, "state overlaps x or y");
+    int rc = check_device(plan);
+    if (rc) return rc;
+    return launch_blocks(plan, x, n, y, state, static_cast<cudaStream_t>(stream_), false, channels,
+                         channels > 1 ? x_stride : 0, channels > 1 ? y_stride : 0, channels > 1 ? state_stride : 0);
 }
 
 int fir_os_launches(fir_os_plan_t plan, int64_t n) {

@@ -243,14 +243,17 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     // everything above reads plan memory only; x, y and the state may belong to the kernel
     // before this one in the stream, which has to be complete from here on
     griddep_wait();
-    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, allow_tma, ucur, tg, gbar);
+    int64_t lu = 0, lun = 0;
+    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(channel_view<REAL>(p, u, lu), lu, cur, bcur, allow_tma, ucur, tg, gbar);
 
     // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
     const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
 
     for (; u < p.nunits; u += stride) {
+        const BlockParams q = channel_view<REAL>(p, u, lu);  // this unit's channel
         const int64_t un = u + stride;
-        if (un < p.nunits) onxt = stage_unit<LOGN, REAL>(p, un, nxt, bnxt, allow_tma, unxt, tg, gbar);
+        if (un < p.nunits)
+            onxt = stage_unit<LOGN, REAL>(channel_view<REAL>(p, un, lun), lun, nxt, bnxt, allow_tma, unxt, tg, gbar);
         if (ucur) {
             const bool ok = mbar_wait_bounded(bcur, pcur);
             pcur ^= 1u;
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
                 // gather this unit with plain loads instead
                 if (tg == 0) atomicExch(p.err, 1);
                 allow_tma = false;
-                ocur = stage_unit<LOGN, REAL>(p, u, cur, bcur, false, ucur, tg, gbar);
+                ocur = stage_unit<LOGN, REAL>(q, lu, cur, bcur, false, ucur, tg, gbar);
             }
         }
 
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = sc[e * T];
         }
-        if (p.fuse_state && u == 0) write_state<LOGN, REAL>(p, cur, tg);
+        if (q.fuse_state && lu == 0) write_state<LOGN, REAL>(q, cur, tg);
 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
@@ -295,12 +298,12 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
         fft_tm<LOGN, 0, true>(v, b0, b1, nullptr, tma, j, gbar);
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
-        const int64_t blk = REAL ? 2 * (u * C::F + f) : (u * C::F + f);
-        const int64_t o0 = blk * p.L - (p.M - 1) + j;  // output index of element e = 0
-        const bool whole = o0 + (int64_t)(15 * T) + (REAL ? p.L : 0) < p.n;
+        const int64_t blk = REAL ? 2 * (lu * C::F + f) : (lu * C::F + f);
+        const int64_t o0 = blk * q.L - (q.M - 1) + j;  // output index of element e = 0
+        const bool whole = o0 + (int64_t)(15 * T) + (REAL ? q.L : 0) < q.n;
         if constexpr (REAL) {
-            float *y = static_cast<float *>(p.y) + o0;
-            float *y2 = y + p.L;
+            float *y = static_cast<float *>(q.y) + o0;
+            float *y2 = y + q.L;
             if (whole) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -312,12 +315,12 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     if (e >= e_keep) {
-                        if (o0 + e * T < p.n) st_cs(y + e * T, v[e].x);
-                        if (o0 + e * T + p.L < p.n) st_cs(y2 + e * T, v[e].y);
+                        if (o0 + e * T < q.n) st_cs(y + e * T, v[e].x);
+                        if (o0 + e * T + q.L < q.n) st_cs(y2 + e * T, v[e].y);
                     }
             }
         } else {
-            float2 *y = static_cast<float2 *>(p.y) + o0;
+            float2 *y = static_cast<float2 *>(q.y) + o0;
             if (whole) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    if (e >= e_keep && o0 + e * T < p.n) st_cs(y + e * T, v[e]);
+                    if (e >= e_keep && o0 + e * T < q.n) st_cs(y + e * T, v[e]);
             }
         }
         gbar.sync();  // `cur` and the exchange buffer are free for the next unit

@@ -349,6 +349,14 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, float2 a, float2 b) {
                  "f"(b.x), "f"(b.y));
 }
 
+// One complex value (two columns) of this thread's lane.
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, float2 &a) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=f"(a.x), "=f"(a.y) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, float2 a) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "f"(a.x), "f"(a.y));
+}
+
 // --------------------------------------------------------------------------- group barriers
 // A CTA may run several independent thread groups; each synchronises on its own hardware
 // barrier (id >= 1; id 0 is __syncthreads).  NT = threads in the group (a multiple of 32).

@@ -17,13 +17,34 @@ struct BlockParams {
     const float2 *twa;     // resident / pair kernels: W_N^{r c} at [c * 128 + r] (c < C),
                            // then W_N^{128 k} at [C * 128 + k] (k < N / 128)
     int *err;              // device error word (set to 1 when a bounded wait ran out)
-    int64_t n;             // samples in this call
-    int64_t nunits;        // work units (block groups / blocks / block pairs)
+    int64_t n;             // samples in this call (per channel)
+    int64_t nunits;        // work units of all channels (block groups / blocks / block pairs)
+    int64_t upc;           // work units per channel; unit u is unit u mod upc of channel u / upc
+    int64_t x_stride;      // samples between channels' x, y and state (0 for one channel)
+    int64_t y_stride;
+    int64_t s_stride;
     int M;                 // taps
     int L;                 // block length N - M + 1
     int fuse_state;        // the kernel writes S0' itself (else a state kernel follows)
     int no_bulk;           // gather every unit with plain loads (x in page-locked host memory)
 };
+
+#ifdef __CUDACC__
+// The single-stream view of work unit u of a (possibly multi-channel) call: x, y and the
+// state of u's channel, and lu, the unit's index within that channel.
+template <bool REAL>
+__device__ __forceinline__ BlockParams channel_view(const BlockParams &p, int64_t u, int64_t &lu) {
+    constexpr int64_t SB = REAL ? 4 : 8;
+    BlockParams q = p;
+    const int64_t ch = u / p.upc;
+    lu = u - ch * p.upc;
+    q.x = static_cast<const char *>(p.x) + ch * p.x_stride * SB;
+    q.y = static_cast<char *>(p.y) + ch * p.y_stride * SB;
+    if (p.state) q.state = static_cast<char *>(p.state) + ch * p.s_stride * SB;
+    q.nunits = p.upc;
+    return q;
+}
+#endif
 
 struct KernelEntry {
     const void *func = nullptr;  // __global__ function

@@ -17,18 +17,22 @@
 // fos_resident.cuh with c' as the sub-transform index), reads the whole input window (from L2;
 // each CTA prefetches half of the next window), and exchanges P values once per block:
 //
-//   phase A   thread (s, r) owns b = r + 128 (8 s + i), i = 0..7: loads the 16 points of every
-//             b, the radix-2 step for its kappa, the 8-point DFTs, the twiddles W_N^{bc}.
+//   phase A   thread (s, r) takes b = r + 128 m for m = 16 rho + 4 s + i (rho < 2, i < 4):
+//             loads the 16 points of every b, the radix-2 step for its kappa, the 8-point DFTs,
+//             the twiddles W_N^{bc}.
 //   phase B   the P-point filtering of fos_resident.cuh for its 8 sub-transforms.
 //   [cluster barrier: both CTAs are done with phase B, so each may write into the other's
 //    exchange buffers]
-//   phase C1  W_N^{-bc} and the 8-point inverse DFT over c' give P_kappa[a', b].  CTA kappa
-//             finishes the outputs for b in [2048 kappa, 2048 kappa + 2048): rows s = 2 kappa,
-//             2 kappa + 1 keep their P values in their lane, the other rows store theirs into
-//             the other CTA's shared memory (128 KB, distributed shared memory).
+//   phase C1  thread (s, r) takes m = 8 s + i (i < 8): W_N^{-bc} and the 8-point inverse DFT
+//             over c' give P_kappa[a', b].  CTA kappa finishes the outputs for b in
+//             [2048 kappa, 2048 kappa + 2048) (m in [16 kappa, 16 kappa + 16)): rows
+//             s = 2 kappa, 2 kappa + 1 keep their P values in their lane, the other rows store
+//             theirs into the other CTA's shared memory (128 KB, distributed shared memory).
 //   [cluster barrier: the values have landed]
-//   phase C2  all 512 threads combine P_0 and P_1 for the CTA's 2048 values of b (4 values of
-//             m per thread) and store R[t] for t >= M - 1 (step 5).
+//   phase C2  with phase A's assignment of m: for its 4 values of m in this CTA's range each
+//             thread combines P_0 and P_1 and stores R[t] for t >= M - 1 (step 5).  Phase A of
+//             the next block runs fused with it: every m starts with the next block's loads,
+//             and the slots a thread combines are the ones it then refills.
 //
 // The two cluster barriers are the only waits on the other CTA; both CTAs take the same
 // blocks (one per cluster, round-robin) and so pass the same barriers.  Real input packs two
@@ -61,52 +65,6 @@ struct PairCfg {
 };
 
 __device__ __forceinline__ int recv_index(int a, int m, int r) { return (a * 16 + (m & 15)) * 128 + r; }
-
-template <bool REAL>
-__device__ __forceinline__ void pair_phase_a(const BlockParams &p, int64_t u, uint32_t kappa, uint32_t tlane,
-                                             int s, int r, const float2 *hi_s, const float2 *wr_s) {
-    using Q = PairCfg<REAL>;
-    constexpr int P = Q::P, HI = Q::HI;
-    const int64_t blk = REAL ? 2 * u : u;
-    const int64_t start = blk * p.L - (p.M - 1);
-    const bool interior = start >= 0 && start + Q::N + (REAL ? p.L : 0) <= p.n;
-    float2 wr[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) wr[c] = wr_s[(kappa + 2 * c) * 128 + r];
-#pragma unroll 1
-    for (int st = 0; st < 4; ++st) {
-        const int i0 = (st & 1) + 4 * (st >> 1);
-        float2 v[2][8];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int b = r + 128 * (8 * s + i0 + 2 * h);
-            float2 x[16];
-#pragma unroll
-            for (int a = 0; a < 16; ++a) x[a] = load_point<REAL>(p, start + P * a + b, interior);
-            if (kappa == 0) {
-#pragma unroll
-                for (int a = 0; a < 8; ++a) v[h][a] = cadd(x[a], x[a + 8]);
-            } else {
-#pragma unroll
-                for (int a = 0; a < 8; ++a) v[h][a] = ctw_dyn<16, -1>(csub(x[a], x[a + 8]), a);
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = 8 * s + i0 + 2 * h;
-            dft<8, -1>(v[h]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int cc = (int)kappa + 2 * c;
-                if (cc != 0) v[h][c] = cmul(v[h][c], cmul(wr[c], hi_s[(m * cc) & (HI - 1)]));
-            }
-        }
-        const uint32_t col = step_col(s, i0);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) tmem_st4(tlane + 64u * c + col, v[0][c], v[1][c]);
-    }
-    tmem_wait_st();
-}
 
 template <bool REAL>
 __device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, int s, int r, const float2 *hi_s,
@@ -151,52 +109,86 @@ __device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, in
     tmem_wait_st();
 }
 
+// Phase C2 of unit uc (when uc >= 0) fused with phase A of unit ua (when ua >= 0).  Thread
+// (s, r) takes the 8 values of m = 16 rho + 4 s + i (rho = 0, 1; i < 4): for those in this
+// CTA's range (rho = kappa) it first combines P_0 and P_1 and stores R (step 5), reading the
+// slots (a', m) that it then overwrites with unit ua's values (c', m); the other range's slots
+// were freed by phase C1.  Each m starts with unit ua's 16 loads, so their latency overlaps the
+// combine and the stores.
 template <bool REAL>
-__device__ __forceinline__ void pair_phase_c2(const BlockParams &p, int64_t u, uint32_t kappa, uint32_t tlane,
-                                              int s, int r, const float2 *recv) {
+__device__ __forceinline__ void pair_phase_c2a(const BlockParams &pc, int64_t uc, const BlockParams &pa,
+                                               int64_t ua, uint32_t kappa, uint32_t tlane, int s, int r,
+                                               const float2 *hi_s, const float2 *wr_s, const float2 *recv) {
     using Q = PairCfg<REAL>;
-    constexpr int P = Q::P;
-    const int64_t blk = REAL ? 2 * u : u;
-    const int64_t start = blk * p.L - (p.M - 1);  // output index of R[0]
-    const bool whole = start + Q::N + (REAL ? p.L : 0) <= p.n;
-    const int keep = p.M - 1;
-    // this thread: m = 16 kappa + 4 s + i, i = 0..3, taken as the slot pairs (i, i + 2)
+    constexpr int P = Q::P, HI = Q::HI;
+    // uc, ua: unit indices within the channels of the views pc and pa
+    const int64_t sc = (REAL ? 2 * uc : uc) * pc.L - (pc.M - 1);  // output index of R[0] of unit uc
+    const bool whole = sc + Q::N + (REAL ? pc.L : 0) <= pc.n;
+    const int keep = pc.M - 1;
+    const int64_t sa = (REAL ? 2 * ua : ua) * pa.L - (pa.M - 1);  // xt index of E[0] of unit ua
+    const bool interior = sa >= 0 && sa + Q::N + (REAL ? pa.L : 0) <= pa.n;
+    float2 wr[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) wr[c] = wr_s[(kappa + 2 * c) * 128 + r];
 #pragma unroll 1
-    for (int i0 = 0; i0 < 2; ++i0) {
-        const int m0 = 16 * (int)kappa + 4 * s + i0;  // and m0 + 2
-        const uint32_t col = 2u * (uint32_t)(16 * (m0 & 1) + (m0 >> 1));
-        float2 pown[2][8];
+    for (int q = 0; q < 8; ++q) {
+        const int rho = (q < 4) ? (int)kappa : 1 - (int)kappa;
+        const int m = 16 * rho + 4 * s + (q & 3);
+        const int b = r + 128 * m;
+        const uint32_t col = 2u * (uint32_t)(16 * (m & 1) + (m >> 1));  // slot (0, m); + 64 per a' or c'
+        float2 x[16];
+        if (ua >= 0) {
 #pragma unroll
-        for (int a = 0; a < 8; ++a) tmem_ld4(tlane + 64u * a + col, pown[0][a], pown[1][a]);
-        tmem_wait_ld();
+            for (int a = 0; a < 16; ++a) x[a] = load_point<REAL>(pa, sa + P * a + b, interior);
+        }
+        if (q < 4 && uc >= 0) {
+            float2 pown[8];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int m = m0 + 2 * h2;
-            const int b = r + 128 * m;
+            for (int a = 0; a < 8; ++a) tmem_ld2(tlane + 64u * a + col, pown[a]);
+            tmem_wait_ld();
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
                 const float2 other = recv[recv_index(a, m, r)];
-                const float2 p0 = kappa == 0 ? pown[h2][a] : other;
-                const float2 p1 = kappa == 0 ? other : pown[h2][a];
-                const float2 q = ctw_dyn<16, +1>(p1, a);  // W_16^{-a} P_1
+                const float2 p0 = kappa == 0 ? pown[a] : other;
+                const float2 p1 = kappa == 0 ? other : pown[a];
+                const float2 w = ctw_dyn<16, +1>(p1, a);  // W_16^{-a'} P_1
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float2 val = h == 0 ? cadd(p0, q) : csub(p0, q);
+                    const float2 val = h == 0 ? cadd(p0, w) : csub(p0, w);
                     const int t = P * (a + 8 * h) + b;
                     if (t < keep) continue;
-                    const int64_t o = start + t;
+                    const int64_t o = sc + t;
                     if constexpr (REAL) {
-                        float *y = static_cast<float *>(p.y);
-                        if (whole || o < p.n) st_cs(y + o, val.x);
-                        if (whole || o + p.L < p.n) st_cs(y + o + p.L, val.y);
+                        float *y = static_cast<float *>(pc.y);
+                        if (whole || o < pc.n) st_cs(y + o, val.x);
+                        if (whole || o + pc.L < pc.n) st_cs(y + o + pc.L, val.y);
                     } else {
-                        float2 *y = static_cast<float2 *>(p.y);
-                        if (whole || o < p.n) st_cs(y + o, val);
+                        float2 *y = static_cast<float2 *>(pc.y);
+                        if (whole || o < pc.n) st_cs(y + o, val);
                     }
                 }
             }
         }
+        if (ua >= 0) {
+            float2 v[8];
+            if (kappa == 0) {
+#pragma unroll
+                for (int a = 0; a < 8; ++a) v[a] = cadd(x[a], x[a + 8]);
+            } else {
+#pragma unroll
+                for (int a = 0; a < 8; ++a) v[a] = ctw_dyn<16, -1>(csub(x[a], x[a + 8]), a);
+            }
+            dft<8, -1>(v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int cc = (int)kappa + 2 * c;
+                if (cc != 0) v[c] = cmul(v[c], cmul(wr[c], hi_s[(m * cc) & (HI - 1)]));
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) tmem_st2(tlane + 64u * c + col, v[c]);
+        }
     }
+    if (ua >= 0) tmem_wait_st();
 }
 
 template <bool REAL>
@@ -219,9 +211,10 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     const GroupBarrier<256> gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
-    int64_t u = cluster_id_x();
+    int64_t u = cluster_id_x(), lu = 0, lun = 0;
     const int64_t ncl = nclusters_x();
-    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, u, tid, (int)kappa, 2);  // a hint
+    BlockParams q = u < p.nunits ? channel_view<REAL>(p, u, lu) : p;  // unit u's channel
+    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(q, lu, tid, (int)kappa, 2);  // a hint
     if (warp == 0) {
         tmem_alloc(tm_slot, Q::TM_COLS);
         tmem_relinquish();
@@ -236,29 +229,33 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
+    if (u < p.nunits) pair_phase_c2a<REAL>(q, -1, q, lu, kappa, tlane, s, r, hi_s, wr_s, bufs);  // phase A of the first unit
     for (; u < p.nunits; u += ncl) {
-        pair_phase_a<REAL>(p, u, kappa, tlane, s, r, hi_s, wr_s);
         tmem_fence_before_sync();
         __syncthreads();
         tmem_fence_after_sync();
         const int64_t un = u + ncl;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, un, tid, (int)kappa, 2);
+        const BlockParams qn = un < p.nunits ? channel_view<REAL>(p, un, lun) : p;
+        if (un < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(qn, lun, tid, (int)kappa, 2);
         phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2);
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
         tmem_fence_after_sync();
-        if (p.fuse_state && u == 0 && kappa == 0) {
-            // only unit 0 reads S0 (fuse_state), and n >= M - 1: S0' = the last M-1 samples of x
+        if (q.fuse_state && lu == 0 && kappa == 0) {
+            // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
+            // last M-1 samples of the channel's x
             using T_ = typename std::conditional<REAL, float, float2>::type;
-            const T_ *x = static_cast<const T_ *>(p.x);
-            T_ *st = static_cast<T_ *>(p.state);
-            for (int t = tid; t < p.M - 1; t += Q::THREADS) st[t] = x[p.n - (p.M - 1) + t];
+            const T_ *x = static_cast<const T_ *>(q.x);
+            T_ *st = static_cast<T_ *>(q.state);
+            for (int t = tid; t < q.M - 1; t += Q::THREADS) st[t] = x[q.n - (q.M - 1) + t];
         }
         pair_phase_c1<REAL>(kappa, tlane, s, r, hi_s, wr_s, peer_recv);
         tmem_fence_before_sync();
         cluster_sync();  // the other CTA's P values have landed in bufs
         tmem_fence_after_sync();
-        pair_phase_c2<REAL>(p, u, kappa, tlane, s, r, bufs);
+        pair_phase_c2a<REAL>(q, lu, qn, un < p.nunits ? lun : -1, kappa, tlane, s, r, hi_s, wr_s, bufs);
+        q = qn;
+        lu = lun;
     }
 
     tmem_fence_before_sync();

@@ -29,9 +29,9 @@
 //   phase C  the ownership of phase A: multiply by W_N^{-bc}; the C-point inverse DFTs over
 //            c give R[P a + b] for every a; R[t] with t >= M - 1 is stored (step 5).
 //
-// Phase A of a thread writes exactly the columns that its phase C read, so phase C of one
-// block and phase A of the next need no barrier between them; two CTA barriers per block
-// order A -> B -> C.  Real input packs two consecutive blocks into one complex transform, as
+// Phase A of a thread writes exactly the columns that its phase C reads, so phase C of one
+// block and phase A of the next run fused, step by step, with the next block's loads issued
+// first; two CTA barriers per block order A -> B -> C.  Real input packs two consecutive blocks into one complex transform, as
 // in the other kernels.  Grid: persistent, one CTA per SM (the Tensor Memory allocation),
 // blocks taken round-robin.  The kernel has no waits on other CTAs or on copies.
 #include <type_traits>
@@ -63,86 +63,80 @@ struct ResidentCfg {
     static_assert(TL::SMEM_ENTRIES == FftShape<LOGP>::TW_ENTRIES, "all pass twiddles in shared memory");
 };
 
-// Phase A: gather, C-point DFTs over a, twiddle, into this thread's lane.
+// Phase C of unit uc (when uc >= 0) and phase A of unit ua (when ua >= 0), fused step by
+// step.  Phase A writes exactly the Tensor Memory columns of this thread that its phase C
+// reads, so each step first issues the loads of unit ua, then reads unit uc's values, does the
+// inverse twiddle, the C-point inverse DFTs and the discard-and-store (step 5), and finally
+// the C-point DFTs over a and the forward twiddle of unit ua into the same columns: the load
+// latency overlaps the inverse work and the stores.
 template <int LOGN, bool REAL>
-__device__ __forceinline__ void phase_a(const BlockParams &p, int64_t u, uint32_t tlane, int s, int r,
-                                        const float2 *hi_s, const float2 *wr_s) {
+__device__ __forceinline__ void phase_ca(const BlockParams &pc, int64_t uc, const BlockParams &pa, int64_t ua,
+                                         uint32_t tlane, int s, int r, const float2 *hi_s, const float2 *wr_s) {
     using R_ = ResidentCfg<LOGN, REAL>;
     constexpr int C = R_::C, P = R_::P, HI = R_::HI;
-    const int64_t blk = REAL ? 2 * u : u;
-    const int64_t start = blk * p.L - (p.M - 1);
-    const bool interior = start >= 0 && start + R_::N + (REAL ? p.L : 0) <= p.n;
+    // uc, ua: unit indices within the channels of the views pc and pa
+    const int64_t sc = (REAL ? 2 * uc : uc) * pc.L - (pc.M - 1);  // output index of R[0] of unit uc
+    const bool whole = sc + R_::N + (REAL ? pc.L : 0) <= pc.n;
+    const int keep = pc.M - 1;
+    const int64_t sa = (REAL ? 2 * ua : ua) * pa.L - (pa.M - 1);  // xt index of E[0] of unit ua
+    const bool interior = sa >= 0 && sa + R_::N + (REAL ? pa.L : 0) <= pa.n;
     float2 wr[C];
 #pragma unroll
     for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
-#pragma unroll
+#pragma unroll 1
     for (int st = 0; st < 4; ++st) {
         const int i0 = (st & 1) + 4 * (st >> 1);  // 0, 1, 4, 5: steps i0 and i0 + 2
-        float2 v[2][C];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int b = r + 128 * (8 * s + i0 + 2 * h);
-#pragma unroll
-            for (int a = 0; a < C; ++a) v[h][a] = load_point<REAL>(p, start + P * a + b, interior);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = 8 * s + i0 + 2 * h;
-            dft<C, -1>(v[h]);
-#pragma unroll
-            for (int c = 1; c < C; ++c) v[h][c] = cmul(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
-        }
         const uint32_t col = step_col(s, i0);
+        float2 xa[2][C];
+        if (ua >= 0) {
 #pragma unroll
-        for (int c = 0; c < C; ++c) tmem_st4(tlane + 64u * c + col, v[0][c], v[1][c]);
-    }
-    tmem_wait_st();
-}
-
-// Phase C: inverse twiddle, C-point inverse DFTs over c, discard, store.
-template <int LOGN, bool REAL>
-__device__ __forceinline__ void phase_c(const BlockParams &p, int64_t u, uint32_t tlane, int s, int r,
-                                        const float2 *hi_s, const float2 *wr_s) {
-    using R_ = ResidentCfg<LOGN, REAL>;
-    constexpr int C = R_::C, P = R_::P, HI = R_::HI;
-    const int64_t blk = REAL ? 2 * u : u;
-    const int64_t start = blk * p.L - (p.M - 1);  // output index of R[0]
-    const bool whole = start + R_::N + (REAL ? p.L : 0) <= p.n;
-    const int keep = p.M - 1;
-    float2 wr[C];
+            for (int h = 0; h < 2; ++h) {
+                const int b = r + 128 * (8 * s + i0 + 2 * h);
 #pragma unroll
-    for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
+                for (int a = 0; a < C; ++a) xa[h][a] = load_point<REAL>(pa, sa + P * a + b, interior);
+            }
+        }
+        if (uc >= 0) {
+            float2 v[2][C];
 #pragma unroll
-    for (int st = 0; st < 4; ++st) {
-        const int i0 = (st & 1) + 4 * (st >> 1);
-        const uint32_t col = step_col(s, i0);
-        float2 v[2][C];
+            for (int c = 0; c < C; ++c) tmem_ld4(tlane + 64u * c + col, v[0][c], v[1][c]);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < C; ++c) tmem_ld4(tlane + 64u * c + col, v[0][c], v[1][c]);
-        tmem_wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                const int m = 8 * s + i0 + 2 * h;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = 8 * s + i0 + 2 * h;
+                for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+                dft<C, +1>(v[h]);
+                const int b = r + 128 * m;
 #pragma unroll
-            for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
-            dft<C, +1>(v[h]);
-            const int b = r + 128 * m;
-#pragma unroll
-            for (int a = 0; a < C; ++a) {
-                const int t = P * a + b;
-                if (t < keep) continue;
-                const int64_t o = start + t;
-                if constexpr (REAL) {
-                    float *y = static_cast<float *>(p.y);
-                    if (whole || o < p.n) st_cs(y + o, v[h][a].x);
-                    if (whole || o + p.L < p.n) st_cs(y + o + p.L, v[h][a].y);
-                } else {
-                    float2 *y = static_cast<float2 *>(p.y);
-                    if (whole || o < p.n) st_cs(y + o, v[h][a]);
+                for (int a = 0; a < C; ++a) {
+                    const int t = P * a + b;
+                    if (t < keep) continue;
+                    const int64_t o = sc + t;
+                    if constexpr (REAL) {
+                        float *y = static_cast<float *>(pc.y);
+                        if (whole || o < pc.n) st_cs(y + o, v[h][a].x);
+                        if (whole || o + pc.L < pc.n) st_cs(y + o + pc.L, v[h][a].y);
+                    } else {
+                        float2 *y = static_cast<float2 *>(pc.y);
+                        if (whole || o < pc.n) st_cs(y + o, v[h][a]);
+                    }
                 }
             }
         }
+        if (ua >= 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = 8 * s + i0 + 2 * h;
+                dft<C, -1>(xa[h]);
+#pragma unroll
+                for (int c = 1; c < C; ++c) xa[h][c] = cmul(xa[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+            }
+#pragma unroll
+            for (int c = 0; c < C; ++c) tmem_st4(tlane + 64u * c + col, xa[0][c], xa[1][c]);
+        }
     }
+    if (ua >= 0) tmem_wait_st();
 }
 
 template <int LOGN, bool REAL>
@@ -162,8 +156,9 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     const GroupBarrier<R_::GT> gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
-    int64_t u = blockIdx.x;
-    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, u, tid);  // a hint only
+    int64_t u = blockIdx.x, lu = 0, lun = 0;
+    BlockParams q = u < p.nunits ? channel_view<REAL>(p, u, lu) : p;  // unit u's channel
+    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(q, lu, tid);  // a hint only
     if (warp == 0) {
         tmem_alloc(tm_slot, R_::TM_COLS);
         tmem_relinquish();
@@ -178,25 +173,30 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
+    if (u < p.nunits) phase_ca<LOGN, REAL>(q, -1, q, lu, tlane, s, r, hi_s, wr_s);  // phase A of the first unit
     for (; u < p.nunits; u += gridDim.x) {
-        phase_a<LOGN, REAL>(p, u, tlane, s, r, hi_s, wr_s);
         tmem_fence_before_sync();
         __syncthreads();  // every (b, c) of the block is in Tensor Memory; S0 has been read
         tmem_fence_after_sync();
-        if (p.fuse_state && u == 0) {
-            // only unit 0 reads S0 (fuse_state), and n >= M - 1: S0' = the last M-1 samples of x
+        if (q.fuse_state && lu == 0) {
+            // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
+            // last M-1 samples of the channel's x
             using T_ = typename std::conditional<REAL, float, float2>::type;
-            const T_ *x = static_cast<const T_ *>(p.x);
-            T_ *st = static_cast<T_ *>(p.state);
-            for (int t = tid; t < p.M - 1; t += R_::THREADS) st[t] = x[p.n - (p.M - 1) + t];
+            const T_ *x = static_cast<const T_ *>(q.x);
+            T_ *st = static_cast<T_ *>(q.state);
+            for (int t = tid; t < q.M - 1; t += R_::THREADS) st[t] = x[q.n - (q.M - 1) + t];
         }
         const int64_t un = u + gridDim.x;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, un, tid);
+        const BlockParams qn = un < p.nunits ? channel_view<REAL>(p, un, lun) : p;
+        if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(qn, lun, tid);
         phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1);
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();
-        phase_c<LOGN, REAL>(p, u, tlane, s, r, hi_s, wr_s);
+        // phase C of this unit with phase A of the next (un is resident in L2 by now)
+        phase_ca<LOGN, REAL>(q, lu, qn, un < p.nunits ? lun : -1, tlane, s, r, hi_s, wr_s);
+        q = qn;
+        lu = lun;
     }
 
     tmem_fence_before_sync();

@@ -35,6 +35,7 @@ SIGNATURES = {
     "fir_os_plan_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _P, _P]),
     "fir_os_execute": (_I, [_P, _P, _I64, _P, _P, _P]),
     "fir_os_execute_host": (_I, [_P, _P, _I64, _P, _P, _P]),
+    "fir_os_execute_batched": (_I, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I, _P]),
     "fir_os_plan_destroy": (_I, [_P]),
     "fir_os_plan_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "fir_os_plan_kernel": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -130,6 +131,21 @@ class Plan:
         """fir_os_execute on CUDA tensors (asynchronous on the stream)."""
         _check(lib().fir_os_execute(self._h, x.data_ptr(), int(x.numel()), y.data_ptr(),
                                     _ptr(state), _stream_handle(stream)))
+        return y
+
+    def execute_batched(self, x, y, state, stream=None):
+        """fir_os_execute_batched on 2-D CUDA tensors (channels, n_samples) whose rows may be
+        strided (contiguous within a row); state is (channels, M-1) or None when M == 1."""
+        if x.dim() != 2 or y.shape != x.shape:
+            raise ValueError("x and y must be 2-D tensors of the same shape (channels, n)")
+        for t in (x, y) + ((state,) if state is not None else ()):
+            if t.stride(1) != 1:
+                raise ValueError("rows must be contiguous")
+        channels, n = x.shape
+        ss = state.stride(0) if state is not None else 0
+        _check(lib().fir_os_execute_batched(self._h, x.data_ptr(), int(x.stride(0)), y.data_ptr(),
+                                            int(y.stride(0)), _ptr(state), int(ss), int(n),
+                                            int(channels), _stream_handle(stream)))
         return y
 
     def execute_host(self, x, y, state, stream=None):

@@ -105,6 +105,29 @@ int fir_os_execute(fir_os_plan_t plan, const void *x_dev, int64_t n_samples, voi
                    void *state_dev, void *stream);
 
 /*
+ * fir_os_execute_batched -- fir_os_execute over `channels` independent streams that share the
+ * plan's filter, in one launch (a bank of identical filters: the channels of an array, a
+ * multi-channel recording).  The method's page filters one stream; each channel here is
+ * filtered exactly as fir_os_execute filters it (steps 3-5 and the state carry of the claim in
+ * "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法", 主权项).
+ *
+ *   x, y           device memory; channel c's n_samples samples start at x + c * x_stride and
+ *                  y + c * y_stride (strides in samples, >= n_samples when channels > 1)
+ *   state          device memory; channel c's M-1 samples (in/out, oldest first) start at
+ *                  state + c * state_stride (stride >= M-1 when channels > 1); NULL only if M == 1
+ *   n_samples      per channel, >= 0 (0 is a no-op)
+ *   channels       >= 1
+ *   stream         as for fir_os_execute
+ *
+ * Returns FIR_OS_E_INVAL for channels < 1, short or negative strides, or when the extents of x,
+ * y and the state (first to last channel) overlap; FIR_OS_E_ALIGN as fir_os_execute.  Every
+ * channel's output and state equal those of fir_os_execute on that channel alone, bit for bit.
+ */
+int fir_os_execute_batched(fir_os_plan_t plan, const void *x, int64_t x_stride, void *y,
+                           int64_t y_stride, void *state, int64_t state_stride, int64_t n_samples,
+                           int channels, void *stream);
+
+/*
  * fir_os_execute_host -- the same filtering for input and output in HOST memory: step 2
  * and step 6 of the claim (move a chunk to the GPU, filter it, move the result back, repeat
  * while data remains).  Synchronous: returns when y_host and state_host hold the results.

@@ -130,6 +130,7 @@ class Workload:
     h_args: tuple = ()
     h_seed: Optional[int] = None
     description: str = ""
+    channels: int = 1     # independent streams filtered together (each `calls` long)
 
     @property
     def L(self) -> int:
@@ -175,6 +176,15 @@ WORKLOADS = {
                    h_seed=6,
                    description="complex64, H given (N=65536, FFT of M=16385 complex h), "
                                "L=49152, k=2048"),
+    # banks of channels sharing one filter, filtered in one batched call per step
+    "C2x16": Workload("C2x16", False, 1024, 4096, (256 * 3073,), 1, "time", "hamming_lowpass", (0.1,),
+                      description="16 channels of complex64, C2's filter (M=1024, N=4096, L=3073), "
+                                  "k=256 blocks per channel, one batched call",
+                      channels=16),
+    "C4x64": Workload("C4x64", True, 255, 1024, (1 << 20,), 4, "time", "kaiser_bandpass", (8.0, 0.2, 0.3),
+                      description="64 channels of real f32, C4's filter (M=255, N=1024, L=770), "
+                                  "2^20 samples per channel, one batched call",
+                      channels=64),
 }
 
 
@@ -229,6 +239,11 @@ def make_x_shard(w: Workload, g: int) -> np.ndarray:
     if w.real:
         return uniform_real(w.n, seed).astype(np.float32)
     return complex_normal(w.n, seed).astype(np.complex64)
+
+
+def make_x_channels(w: Workload) -> np.ndarray:
+    """The inputs of all channels, shape (channels, n): channel c is make_x_shard(w, c)."""
+    return np.stack([make_x_shard(w, c) for c in range(w.channels)])
 
 
 def make_state0(w: Workload) -> np.ndarray:
