@@ -319,7 +319,8 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    FOS_CUDA(cudaLaunchKernelExC(&cfg, p->kernel.func, args), "block kernel launch");
+    const void *func = channels > 1 && p->kernel.func_multi ? p->kernel.func_multi : p->kernel.func;
+    FOS_CUDA(cudaLaunchKernelExC(&cfg, func, args), "block kernel launch");
     if (!bp.fuse_state && p->M > 1) {
         if (real)
             fos_state_kernel<float><<<channels, 1024, 0, stream>>>(static_cast<const float *>(x), n,
@@ -430,6 +431,11 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
         cudaError_t e = cudaFuncSetAttribute(p->kernel.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              p->kernel.smem);
         if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+        if (p->kernel.func_multi) {
+            e = cudaFuncSetAttribute(p->kernel.func_multi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     p->kernel.smem);
+            if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+        }
         if (p->kernel.cluster == 1) {
             int per_sm = 0;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, p->kernel.func, p->kernel.threads,
@@ -438,10 +444,7 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
             if (per_sm < 1) return bail(fail(FIR_OS_E_UNSUPPORTED, "block kernel does not fit an SM"));
             p->max_units_in_flight = per_sm * p->sms;
         } else {
-            if (p->kernel.cluster > 8) {
-                e = cudaFuncSetAttribute(p->kernel.func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(cluster size)"));
-            }
+
             cudaLaunchConfig_t cfg{};
             cfg.gridDim = dim3(p->kernel.cluster * 64);
             cfg.blockDim = dim3(p->kernel.threads);

@@ -78,7 +78,8 @@ struct BlockCfg {
 // `bar`; used_tma = true) when the 16-byte-rounded byte range lies inside x; otherwise every
 // thread gathers with plain loads and the CTA synchronises (used_tma = false).
 template <int LOGN, bool REAL>
-__device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsigned char *buf, uint64_t *bar,
+__device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, int64_t u, unsigned char *buf,
+                                          uint64_t *bar,
                                           bool allow_tma, bool &used_tma, int tid,
                                           const typename BlockCfg<LOGN, REAL>::Bar &gbar) {
     using C = BlockCfg<LOGN, REAL>;
@@ -87,7 +88,7 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
     const int64_t start = u * span - (p.M - 1);
     const int64_t len = (int64_t)(REAL ? 2 * C::F - 1 : C::F - 1) * p.L + C::N;
     if (allow_tma && start >= 0) {
-        const uintptr_t xb = reinterpret_cast<uintptr_t>(p.x);
+        const uintptr_t xb = reinterpret_cast<uintptr_t>(ch.x);
         const uintptr_t a0 = xb + (uintptr_t)start * SB, a1 = a0 + (uintptr_t)len * SB;
         const uintptr_t b0 = a0 & ~uintptr_t(15), b1 = (a1 + 15) & ~uintptr_t(15);
         if (b0 >= xb && b1 <= xb + (uintptr_t)p.n * SB) {
@@ -103,8 +104,8 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
     used_tma = false;
     const int64_t hist = p.M - 1;
     using T_ = typename std::conditional<REAL, float, float2>::type;
-    const T_ *x = static_cast<const T_ *>(p.x);
-    const T_ *s0 = static_cast<const T_ *>(p.state);
+    const T_ *x = static_cast<const T_ *>(ch.x);
+    const T_ *s0 = static_cast<const T_ *>(ch.state);
     T_ *dst = reinterpret_cast<T_ *>(buf);
     // batches of independent loads, so their latencies overlap instead of adding up
     constexpr int U = 8;
@@ -133,12 +134,13 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, int64_t u, unsig
 // S0' = xt[n-(M-1) .. n): samples of x, or (when n < M-1) of S0, which the gather of unit 0
 // left at buffer index (t + M - 1) for xt[t], t < 0.
 template <int LOGN, bool REAL>
-__device__ __forceinline__ void write_state(const BlockParams &p, const unsigned char *buf, int tid) {
+__device__ __forceinline__ void write_state(const BlockParams &p, const Chan &ch, const unsigned char *buf,
+                                            int tid) {
     using C = BlockCfg<LOGN, REAL>;
     using T_ = typename std::conditional<REAL, float, float2>::type;
-    const T_ *x = static_cast<const T_ *>(p.x);
+    const T_ *x = static_cast<const T_ *>(ch.x);
     const T_ *stg = reinterpret_cast<const T_ *>(buf);
-    T_ *st = static_cast<T_ *>(p.state);
+    T_ *st = static_cast<T_ *>(ch.state);
     const int hist = p.M - 1;
     constexpr int U = 8;  // independent loads in flight per thread
     for (int t0 = tid; t0 < hist; t0 += U * C::GT) {
@@ -244,16 +246,21 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     // before this one in the stream, which has to be complete from here on
     griddep_wait();
     int64_t lu = 0, lun = 0;
-    if (u < p.nunits) ocur = stage_unit<LOGN, REAL>(channel_view<REAL>(p, u, lu), lu, cur, bcur, allow_tma, ucur, tg, gbar);
+    if (u < p.nunits) {
+        const int c0 = channel_of(p, u, lu);
+        ocur = stage_unit<LOGN, REAL>(p, chan<REAL>(p, c0), lu, cur, bcur, allow_tma, ucur, tg, gbar);
+    }
 
     // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
     const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
 
     for (; u < p.nunits; u += stride) {
-        const BlockParams q = channel_view<REAL>(p, u, lu);  // this unit's channel
+        const int chu = channel_of(p, u, lu);  // this unit's channel
         const int64_t un = u + stride;
-        if (un < p.nunits)
-            onxt = stage_unit<LOGN, REAL>(channel_view<REAL>(p, un, lun), lun, nxt, bnxt, allow_tma, unxt, tg, gbar);
+        if (un < p.nunits) {
+            const int chn = channel_of(p, un, lun);
+            onxt = stage_unit<LOGN, REAL>(p, chan<REAL>(p, chn), lun, nxt, bnxt, allow_tma, unxt, tg, gbar);
+        }
         if (ucur) {
             const bool ok = mbar_wait_bounded(bcur, pcur);
             pcur ^= 1u;
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
                 // gather this unit with plain loads instead
                 if (tg == 0) atomicExch(p.err, 1);
                 allow_tma = false;
-                ocur = stage_unit<LOGN, REAL>(q, lu, cur, bcur, false, ucur, tg, gbar);
+                ocur = stage_unit<LOGN, REAL>(p, chan<REAL>(p, chu), lu, cur, bcur, false, ucur, tg, gbar);
             }
         }
 
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = sc[e * T];
         }
-        if (q.fuse_state && lu == 0) write_state<LOGN, REAL>(q, cur, tg);
+        if (p.fuse_state && lu == 0) write_state<LOGN, REAL>(p, chan<REAL>(p, chu), cur, tg);
 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
@@ -299,11 +306,11 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
         const int64_t blk = REAL ? 2 * (lu * C::F + f) : (lu * C::F + f);
-        const int64_t o0 = blk * q.L - (q.M - 1) + j;  // output index of element e = 0
-        const bool whole = o0 + (int64_t)(15 * T) + (REAL ? q.L : 0) < q.n;
+        const int64_t o0 = blk * p.L - (p.M - 1) + j;  // output index of element e = 0
+        const bool whole = o0 + (int64_t)(15 * T) + (REAL ? p.L : 0) < p.n;
         if constexpr (REAL) {
-            float *y = static_cast<float *>(q.y) + o0;
-            float *y2 = y + q.L;
+            float *y = static_cast<float *>(chan<REAL>(p, chu).y) + o0;
+            float *y2 = y + p.L;
             if (whole) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -315,12 +322,12 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     if (e >= e_keep) {
-                        if (o0 + e * T < q.n) st_cs(y + e * T, v[e].x);
-                        if (o0 + e * T + q.L < q.n) st_cs(y2 + e * T, v[e].y);
+                        if (o0 + e * T < p.n) st_cs(y + e * T, v[e].x);
+                        if (o0 + e * T + p.L < p.n) st_cs(y2 + e * T, v[e].y);
                     }
             }
         } else {
-            float2 *y = static_cast<float2 *>(q.y) + o0;
+            float2 *y = static_cast<float2 *>(chan<REAL>(p, chu).y) + o0;
             if (whole) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    if (e >= e_keep && o0 + e * T < q.n) st_cs(y + e * T, v[e]);
+                    if (e >= e_keep && o0 + e * T < p.n) st_cs(y + e * T, v[e]);
             }
         }
         gbar.sync();  // `cur` and the exchange buffer are free for the next unit

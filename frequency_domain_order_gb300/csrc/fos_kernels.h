@@ -29,25 +29,41 @@ struct BlockParams {
     int no_bulk;           // gather every unit with plain loads (x in page-locked host memory)
 };
 
+// The buffers of one channel of a (possibly multi-channel) call.
+struct Chan {
+    const void *x;
+    void *y;
+    void *state;
+};
+
 #ifdef __CUDACC__
-// The single-stream view of work unit u of a (possibly multi-channel) call: x, y and the
-// state of u's channel, and lu, the unit's index within that channel.
-template <bool REAL>
-__device__ __forceinline__ BlockParams channel_view(const BlockParams &p, int64_t u, int64_t &lu) {
-    constexpr int64_t SB = REAL ? 4 : 8;
-    BlockParams q = p;
+// Channel of work unit u, and lu, the unit's index within that channel.  Kernels keep only this
+// index alive and form the channel's pointers (chan) where they use them.  Everything else a
+// kernel needs (n, M, L, ...) is the same for every channel and stays in BlockParams.
+template <bool MULTI = true>
+__device__ __forceinline__ int channel_of(const BlockParams &p, int64_t u, int64_t &lu) {
+    if constexpr (!MULTI) {  // a single-channel instantiation: channel 0, nothing to compute
+        lu = u;
+        return 0;
+    }
     const int64_t ch = u / p.upc;
     lu = u - ch * p.upc;
-    q.x = static_cast<const char *>(p.x) + ch * p.x_stride * SB;
-    q.y = static_cast<char *>(p.y) + ch * p.y_stride * SB;
-    if (p.state) q.state = static_cast<char *>(p.state) + ch * p.s_stride * SB;
-    q.nunits = p.upc;
-    return q;
+    return (int)ch;
+}
+template <bool REAL>
+__device__ __forceinline__ Chan chan(const BlockParams &p, int ch) {
+    constexpr int64_t SB = REAL ? 4 : 8;
+    Chan c;
+    c.x = static_cast<const char *>(p.x) + (int64_t)ch * p.x_stride * SB;
+    c.y = static_cast<char *>(p.y) + (int64_t)ch * p.y_stride * SB;
+    c.state = p.state ? static_cast<char *>(p.state) + (int64_t)ch * p.s_stride * SB : nullptr;
+    return c;
 }
 #endif
 
 struct KernelEntry {
     const void *func = nullptr;  // __global__ function
+    const void *func_multi = nullptr;  // the same for calls of more than one channel, if separate
     int threads = 0;             // threads per CTA
     int smem = 0;                // dynamic shared memory per CTA (bytes)
     int cluster = 1;             // CTAs per cluster (1 = no cluster)

@@ -116,17 +116,17 @@ __device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, in
 // were freed by phase C1.  Each m starts with unit ua's 16 loads, so their latency overlaps the
 // combine and the stores.
 template <bool REAL>
-__device__ __forceinline__ void pair_phase_c2a(const BlockParams &pc, int64_t uc, const BlockParams &pa,
-                                               int64_t ua, uint32_t kappa, uint32_t tlane, int s, int r,
+__device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc, void *yc, int64_t ua,
+                                               const Chan &cha, uint32_t kappa, uint32_t tlane, int s, int r,
                                                const float2 *hi_s, const float2 *wr_s, const float2 *recv) {
     using Q = PairCfg<REAL>;
     constexpr int P = Q::P, HI = Q::HI;
-    // uc, ua: unit indices within the channels of the views pc and pa
-    const int64_t sc = (REAL ? 2 * uc : uc) * pc.L - (pc.M - 1);  // output index of R[0] of unit uc
-    const bool whole = sc + Q::N + (REAL ? pc.L : 0) <= pc.n;
-    const int keep = pc.M - 1;
-    const int64_t sa = (REAL ? 2 * ua : ua) * pa.L - (pa.M - 1);  // xt index of E[0] of unit ua
-    const bool interior = sa >= 0 && sa + Q::N + (REAL ? pa.L : 0) <= pa.n;
+    // uc, ua: unit indices within their channels; yc: uc's channel's output, cha: ua's channel
+    const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
+    const bool whole = sc + Q::N + (REAL ? p.L : 0) <= p.n;
+    const int keep = p.M - 1;
+    const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
+    const bool interior = sa >= 0 && sa + Q::N + (REAL ? p.L : 0) <= p.n;
     float2 wr[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) wr[c] = wr_s[(kappa + 2 * c) * 128 + r];
@@ -139,7 +139,7 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &pc, int64_t uc
         float2 x[16];
         if (ua >= 0) {
 #pragma unroll
-            for (int a = 0; a < 16; ++a) x[a] = load_point<REAL>(pa, sa + P * a + b, interior);
+            for (int a = 0; a < 16; ++a) x[a] = load_point<REAL>(p, cha, sa + P * a + b, interior);
         }
         if (q < 4 && uc >= 0) {
             float2 pown[8];
@@ -159,12 +159,12 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &pc, int64_t uc
                     if (t < keep) continue;
                     const int64_t o = sc + t;
                     if constexpr (REAL) {
-                        float *y = static_cast<float *>(pc.y);
-                        if (whole || o < pc.n) st_cs(y + o, val.x);
-                        if (whole || o + pc.L < pc.n) st_cs(y + o + pc.L, val.y);
+                        float *y = static_cast<float *>(yc);
+                        if (whole || o < p.n) st_cs(y + o, val.x);
+                        if (whole || o + p.L < p.n) st_cs(y + o + p.L, val.y);
                     } else {
-                        float2 *y = static_cast<float2 *>(pc.y);
-                        if (whole || o < pc.n) st_cs(y + o, val);
+                        float2 *y = static_cast<float2 *>(yc);
+                        if (whole || o < p.n) st_cs(y + o, val);
                     }
                 }
             }
@@ -191,7 +191,7 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &pc, int64_t uc
     if (ua >= 0) tmem_wait_st();
 }
 
-template <bool REAL>
+template <bool REAL, bool MULTI>
 __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     using Q = PairCfg<REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
     int64_t u = cluster_id_x(), lu = 0, lun = 0;
     const int64_t ncl = nclusters_x();
-    BlockParams q = u < p.nunits ? channel_view<REAL>(p, u, lu) : p;  // unit u's channel
-    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(q, lu, tid, (int)kappa, 2);  // a hint
+    int chu = u < p.nunits ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
+    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chu), lu, tid, (int)kappa, 2);  // a hint
     if (warp == 0) {
         tmem_alloc(tm_slot, Q::TM_COLS);
         tmem_relinquish();
@@ -229,32 +229,35 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
-    if (u < p.nunits) pair_phase_c2a<REAL>(q, -1, q, lu, kappa, tlane, s, r, hi_s, wr_s, bufs);  // phase A of the first unit
+    if (u < p.nunits)  // phase A of the first unit
+        pair_phase_c2a<REAL>(p, -1, nullptr, lu, chan<REAL>(p, chu), kappa, tlane, s, r, hi_s, wr_s, bufs);
     for (; u < p.nunits; u += ncl) {
         tmem_fence_before_sync();
         __syncthreads();
         tmem_fence_after_sync();
         const int64_t un = u + ncl;
-        const BlockParams qn = un < p.nunits ? channel_view<REAL>(p, un, lun) : p;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(qn, lun, tid, (int)kappa, 2);
+        const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
+        if (un < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, (int)kappa, 2);
         phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2);
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
         tmem_fence_after_sync();
-        if (q.fuse_state && lu == 0 && kappa == 0) {
+        if (p.fuse_state && lu == 0 && kappa == 0) {
             // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
             // last M-1 samples of the channel's x
             using T_ = typename std::conditional<REAL, float, float2>::type;
-            const T_ *x = static_cast<const T_ *>(q.x);
-            T_ *st = static_cast<T_ *>(q.state);
-            for (int t = tid; t < q.M - 1; t += Q::THREADS) st[t] = x[q.n - (q.M - 1) + t];
+            const Chan cu = chan<REAL>(p, chu);
+            const T_ *x = static_cast<const T_ *>(cu.x);
+            T_ *st = static_cast<T_ *>(cu.state);
+            for (int t = tid; t < p.M - 1; t += Q::THREADS) st[t] = x[p.n - (p.M - 1) + t];
         }
         pair_phase_c1<REAL>(kappa, tlane, s, r, hi_s, wr_s, peer_recv);
         tmem_fence_before_sync();
         cluster_sync();  // the other CTA's P values have landed in bufs
         tmem_fence_after_sync();
-        pair_phase_c2a<REAL>(q, lu, qn, un < p.nunits ? lun : -1, kappa, tlane, s, r, hi_s, wr_s, bufs);
-        q = qn;
+        pair_phase_c2a<REAL>(p, lu, chan<REAL>(p, chu).y, un < p.nunits ? lun : -1, chan<REAL>(p, chn), kappa, tlane,
+                             s, r, hi_s, wr_s, bufs);
+        chu = chn;
         lu = lun;
     }
 
@@ -268,7 +271,8 @@ template <bool REAL>
 KernelEntry pair_entry() {
     using Q = PairCfg<REAL>;
     KernelEntry k;
-    k.func = reinterpret_cast<const void *>(&fos_pair_kernel<REAL>);
+    k.func = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, false>);
+    k.func_multi = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, true>);
     k.threads = Q::THREADS;
     k.smem = Q::SMEM_BYTES;
     k.cluster = 2;

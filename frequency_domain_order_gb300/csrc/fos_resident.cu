@@ -70,16 +70,16 @@ struct ResidentCfg {
 // the C-point DFTs over a and the forward twiddle of unit ua into the same columns: the load
 // latency overlaps the inverse work and the stores.
 template <int LOGN, bool REAL>
-__device__ __forceinline__ void phase_ca(const BlockParams &pc, int64_t uc, const BlockParams &pa, int64_t ua,
+__device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void *yc, int64_t ua, const Chan &cha,
                                          uint32_t tlane, int s, int r, const float2 *hi_s, const float2 *wr_s) {
     using R_ = ResidentCfg<LOGN, REAL>;
     constexpr int C = R_::C, P = R_::P, HI = R_::HI;
-    // uc, ua: unit indices within the channels of the views pc and pa
-    const int64_t sc = (REAL ? 2 * uc : uc) * pc.L - (pc.M - 1);  // output index of R[0] of unit uc
-    const bool whole = sc + R_::N + (REAL ? pc.L : 0) <= pc.n;
-    const int keep = pc.M - 1;
-    const int64_t sa = (REAL ? 2 * ua : ua) * pa.L - (pa.M - 1);  // xt index of E[0] of unit ua
-    const bool interior = sa >= 0 && sa + R_::N + (REAL ? pa.L : 0) <= pa.n;
+    // uc, ua: unit indices within their channels; yc: uc's channel's output, cha: ua's channel
+    const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
+    const bool whole = sc + R_::N + (REAL ? p.L : 0) <= p.n;
+    const int keep = p.M - 1;
+    const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
+    const bool interior = sa >= 0 && sa + R_::N + (REAL ? p.L : 0) <= p.n;
     float2 wr[C];
 #pragma unroll
     for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
@@ -93,7 +93,7 @@ __device__ __forceinline__ void phase_ca(const BlockParams &pc, int64_t uc, cons
             for (int h = 0; h < 2; ++h) {
                 const int b = r + 128 * (8 * s + i0 + 2 * h);
 #pragma unroll
-                for (int a = 0; a < C; ++a) xa[h][a] = load_point<REAL>(pa, sa + P * a + b, interior);
+                for (int a = 0; a < C; ++a) xa[h][a] = load_point<REAL>(p, cha, sa + P * a + b, interior);
             }
         }
         if (uc >= 0) {
@@ -114,12 +114,12 @@ __device__ __forceinline__ void phase_ca(const BlockParams &pc, int64_t uc, cons
                     if (t < keep) continue;
                     const int64_t o = sc + t;
                     if constexpr (REAL) {
-                        float *y = static_cast<float *>(pc.y);
-                        if (whole || o < pc.n) st_cs(y + o, v[h][a].x);
-                        if (whole || o + pc.L < pc.n) st_cs(y + o + pc.L, v[h][a].y);
+                        float *y = static_cast<float *>(yc);
+                        if (whole || o < p.n) st_cs(y + o, v[h][a].x);
+                        if (whole || o + p.L < p.n) st_cs(y + o + p.L, v[h][a].y);
                     } else {
-                        float2 *y = static_cast<float2 *>(pc.y);
-                        if (whole || o < pc.n) st_cs(y + o, v[h][a]);
+                        float2 *y = static_cast<float2 *>(yc);
+                        if (whole || o < p.n) st_cs(y + o, v[h][a]);
                     }
                 }
             }
@@ -139,7 +139,7 @@ __device__ __forceinline__ void phase_ca(const BlockParams &pc, int64_t uc, cons
     if (ua >= 0) tmem_wait_st();
 }
 
-template <int LOGN, bool REAL>
+template <int LOGN, bool REAL, bool MULTI>
 __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams p) {
     using R_ = ResidentCfg<LOGN, REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
     int64_t u = blockIdx.x, lu = 0, lun = 0;
-    BlockParams q = u < p.nunits ? channel_view<REAL>(p, u, lu) : p;  // unit u's channel
-    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(q, lu, tid);  // a hint only
+    int chu = u < p.nunits ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
+    if (u < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, chan<REAL>(p, chu), lu, tid);  // a hint only
     if (warp == 0) {
         tmem_alloc(tm_slot, R_::TM_COLS);
         tmem_relinquish();
@@ -173,29 +173,32 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
-    if (u < p.nunits) phase_ca<LOGN, REAL>(q, -1, q, lu, tlane, s, r, hi_s, wr_s);  // phase A of the first unit
+    if (u < p.nunits)  // phase A of the first unit
+        phase_ca<LOGN, REAL>(p, -1, nullptr, lu, chan<REAL>(p, chu), tlane, s, r, hi_s, wr_s);
     for (; u < p.nunits; u += gridDim.x) {
         tmem_fence_before_sync();
         __syncthreads();  // every (b, c) of the block is in Tensor Memory; S0 has been read
         tmem_fence_after_sync();
-        if (q.fuse_state && lu == 0) {
+        if (p.fuse_state && lu == 0) {
             // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
             // last M-1 samples of the channel's x
             using T_ = typename std::conditional<REAL, float, float2>::type;
-            const T_ *x = static_cast<const T_ *>(q.x);
-            T_ *st = static_cast<T_ *>(q.state);
-            for (int t = tid; t < q.M - 1; t += R_::THREADS) st[t] = x[q.n - (q.M - 1) + t];
+            const Chan cu = chan<REAL>(p, chu);
+            const T_ *x = static_cast<const T_ *>(cu.x);
+            T_ *st = static_cast<T_ *>(cu.state);
+            for (int t = tid; t < p.M - 1; t += R_::THREADS) st[t] = x[p.n - (p.M - 1) + t];
         }
         const int64_t un = u + gridDim.x;
-        const BlockParams qn = un < p.nunits ? channel_view<REAL>(p, un, lun) : p;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(qn, lun, tid);
+        const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
+        if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, chan<REAL>(p, chn), lun, tid);
         phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1);
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();
         // phase C of this unit with phase A of the next (un is resident in L2 by now)
-        phase_ca<LOGN, REAL>(q, lu, qn, un < p.nunits ? lun : -1, tlane, s, r, hi_s, wr_s);
-        q = qn;
+        phase_ca<LOGN, REAL>(p, lu, chan<REAL>(p, chu).y, un < p.nunits ? lun : -1, chan<REAL>(p, chn), tlane, s,
+                             r, hi_s, wr_s);
+        chu = chn;
         lu = lun;
     }
 
@@ -209,7 +212,8 @@ template <int LOGN, bool REAL>
 KernelEntry resident_entry() {
     using R_ = ResidentCfg<LOGN, REAL>;
     KernelEntry k;
-    k.func = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL>);
+    k.func = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, false>);
+    k.func_multi = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, true>);
     k.threads = R_::THREADS;
     k.smem = R_::SMEM_BYTES;
     k.cluster = 1;

@@ -18,14 +18,14 @@ __device__ __forceinline__ uint32_t step_col(int s, int i0) {
     return 2u * (uint32_t)(16 * (i0 & 1) + 4 * s + (i0 >> 1));
 }
 
-// xt[t] of the first block of the unit (and, for real data, of the second block at t + L):
-// x inside [0, n), S0 in front of it, zeros after it.
+// xt[t] of the first block of the unit (and, for real data, of the second block at t + L) in
+// channel ch: x inside [0, n), S0 in front of it, zeros after it.
 template <bool REAL>
-__device__ __forceinline__ float2 load_point(const BlockParams &p, int64_t t, bool interior) {
+__device__ __forceinline__ float2 load_point(const BlockParams &p, const Chan &ch, int64_t t, bool interior) {
     if constexpr (REAL) {
-        const float *x = static_cast<const float *>(p.x);
+        const float *x = static_cast<const float *>(ch.x);
         if (interior) return make_float2(x[t], x[t + p.L]);
-        const float *s0 = static_cast<const float *>(p.state);
+        const float *s0 = static_cast<const float *>(ch.state);
         float v[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -39,19 +39,19 @@ __device__ __forceinline__ float2 load_point(const BlockParams &p, int64_t t, bo
         }
         return make_float2(v[0], v[1]);
     } else {
-        const float2 *x = static_cast<const float2 *>(p.x);
+        const float2 *x = static_cast<const float2 *>(ch.x);
         if (interior) return x[t];
         if (t >= 0) return t < p.n ? x[t] : make_float2(0.f, 0.f);
-        if (t >= -(int64_t)(p.M - 1)) return static_cast<const float2 *>(p.state)[p.M - 1 + t];
+        if (t >= -(int64_t)(p.M - 1)) return static_cast<const float2 *>(ch.state)[p.M - 1 + t];
         return make_float2(0.f, 0.f);
     }
 }
 
-// Bulk L2 prefetch of part `part` of `parts` of unit u's input window (the part of the
-// window inside x), split over 16 threads.
+// Bulk L2 prefetch of part `part` of `parts` of the input window of unit u of channel ch (the
+// part of the window inside x), split over 16 threads.
 template <int N, bool REAL>
-__device__ __forceinline__ void prefetch_window(const BlockParams &p, int64_t u, int tid, int part = 0,
-                                                int parts = 1) {
+__device__ __forceinline__ void prefetch_window(const BlockParams &p, const Chan &ch, int64_t u, int tid,
+                                                int part = 0, int parts = 1) {
     constexpr int SB = REAL ? 4 : 8;
     constexpr int NPF = 16;
     if (tid >= NPF) return;
@@ -64,7 +64,7 @@ __device__ __forceinline__ void prefetch_window(const BlockParams &p, int64_t u,
     if (hi > p.n) hi = p.n;
     if (hi <= lo) return;
     // rounded inwards to 16 bytes, so the range stays inside x
-    const uintptr_t xb = reinterpret_cast<uintptr_t>(p.x);
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(ch.x);
     const uintptr_t a0 = (xb + (uintptr_t)lo * SB + 15) & ~uintptr_t(15);
     const uintptr_t a1 = (xb + (uintptr_t)hi * SB) & ~uintptr_t(15);
     if (a1 <= a0) return;
