@@ -353,9 +353,95 @@ int check_device(const fir_os_plan *p) {
     return FIR_OS_OK;
 }
 
+// Device time of one block (real data: one block of a packed pair) in SM-microseconds, measured
+// on a GB300 (152 SMs, 2070 MHz) by timing one call of at least 2048 blocks (about 64 M samples)
+// per N with M - 1 = N/4, N/2 and 3N/4, i.e. L/N = 3/4, 1/2, 1/4 (stored in increasing L/N).
+struct BlockCost {
+    int N;
+    int real;
+    double sm_us[3];  // at L/N = 1/4, 1/2, 3/4
+};
+const BlockCost kBlockCost[] = {
+    {64, 0, {0.0316, 0.0342, 0.0376}},
+    {128, 0, {0.0479, 0.0509, 0.0547}},
+    {256, 0, {0.0897, 0.0942, 0.1003}},
+    {512, 0, {0.2401, 0.2492, 0.2599}},
+    {1024, 0, {0.4956, 0.5105, 0.5334}},
+    {2048, 0, {1.1095, 1.1425, 1.1851}},
+    {4096, 0, {2.4438, 2.5772, 2.6979}},
+    {8192, 0, {6.6633, 7.0034, 7.5149}},
+    {16384, 0, {14.8344, 16.0482, 17.3649}},
+    {32768, 0, {28.8420, 31.9048, 36.4983}},
+    {65536, 0, {81.4112, 89.4854, 100.4466}},
+    {64, 1, {0.0205, 0.0228, 0.0261}},
+    {128, 1, {0.0281, 0.0302, 0.0325}},
+    {256, 1, {0.0479, 0.0509, 0.0539}},
+    {512, 1, {0.1229, 0.1292, 0.1368}},
+    {1024, 1, {0.2538, 0.2622, 0.2780}},
+    {2048, 1, {0.5916, 0.6034, 0.6336}},
+    {4096, 1, {1.4052, 1.4833, 1.5716}},
+    {8192, 1, {3.3590, 3.5340, 3.8174}},
+    {16384, 1, {7.4628, 8.2924, 9.1146}},
+    {32768, 1, {15.4310, 17.4253, 20.7923}},
+    {65536, 1, {43.0190, 47.4605, 53.7230}},
+};
+
+// Predicted throughput (output samples per second, 1e9) of an (M, N) plan on `sms` SMs: L
+// samples per block, the block's SM time interpolated linearly in L/N between the measured
+// points (extrapolated linearly beyond them).
+double predict_gsps(int M, int N, bool real, int sms) {
+    for (const BlockCost &b : kBlockCost) {
+        if (b.N != N || b.real != (real ? 1 : 0)) continue;
+        const int L = N - M + 1;
+        const double f = (double)L / N;
+        const double x0 = f <= 0.5 ? 0.25 : 0.5;
+        const double y0 = f <= 0.5 ? b.sm_us[0] : b.sm_us[1];
+        const double y1 = f <= 0.5 ? b.sm_us[1] : b.sm_us[2];
+        double t = y0 + (y1 - y0) * (f - x0) / 0.25;
+        if (t < 0.5 * b.sm_us[0]) t = 0.5 * b.sm_us[0];
+        return (double)L * sms / t * 1e-3;
+    }
+    return 0.0;
+}
+
 }  // namespace
 
 extern "C" {
+
+int fir_os_predict_gsps(int M, int N, int data_kind, int sms, double *gsps) {
+    if (!gsps) return fail(FIR_OS_E_INVAL, "gsps is NULL");
+    if (data_kind != FIR_OS_REAL && data_kind != FIR_OS_COMPLEX)
+        return fail(FIR_OS_E_INVAL, "data_kind %d is neither FIR_OS_REAL nor FIR_OS_COMPLEX", data_kind);
+    if (sms < 0) return fail(FIR_OS_E_INVAL, "sms < 0");
+    if (N < 64 || N > 65536 || (N & (N - 1)) != 0)
+        return fail(FIR_OS_E_UNSUPPORTED, "N = %d is not a power of two in [64, 65536]", N);
+    if (M < 1 || M > N) return fail(FIR_OS_E_UNSUPPORTED, "M = %d must be in [1, N = %d]", M, N);
+    *gsps = predict_gsps(M, N, data_kind == FIR_OS_REAL, sms ? sms : 152);
+    return FIR_OS_OK;
+}
+
+int fir_os_choose_n(int M, int data_kind, int sms, int *N, double *gsps) {
+    if (!N) return fail(FIR_OS_E_INVAL, "N is NULL");
+    if (data_kind != FIR_OS_REAL && data_kind != FIR_OS_COMPLEX)
+        return fail(FIR_OS_E_INVAL, "data_kind %d is neither FIR_OS_REAL nor FIR_OS_COMPLEX", data_kind);
+    if (sms < 0) return fail(FIR_OS_E_INVAL, "sms < 0");
+    if (M < 1) return fail(FIR_OS_E_INVAL, "M = %d < 1", M);
+    if (M > 65536) return fail(FIR_OS_E_UNSUPPORTED, "M = %d > 65536", M);
+    int best = 0;
+    double best_g = -1.0;
+    for (int n = 64; n <= 65536; n *= 2) {
+        if (n < M) continue;
+        const double g = predict_gsps(M, n, data_kind == FIR_OS_REAL, sms ? sms : 152);
+        if (g > best_g) {
+            best_g = g;
+            best = n;
+        }
+    }
+    *N = best;
+    if (gsps) *gsps = best_g;
+    return FIR_OS_OK;
+}
+
 
 const char *fir_os_status_string(int status) {
     switch (status) {

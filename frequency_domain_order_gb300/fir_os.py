@@ -43,12 +43,28 @@ SIGNATURES = {
     "fir_os_device_status": (_I, [_P, _P]),
     "fir_os_launches": (_I, [_P, _I64]),
     "fir_os_frequency_response_noalloc": (_I, [_P, _I, _I, _I, _P, _P]),
+    "fir_os_choose_n": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
+    "fir_os_predict_gsps": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_double)]),
     "fir_os_status_string": (ctypes.c_char_p, [_I]),
     "fir_os_last_error": (ctypes.c_char_p, []),
 }
 
 _lock = threading.Lock()
 _lib = None
+
+
+def choose_n(M: int, real: bool = False, sms: int = 0):
+    """fir_os_choose_n: (N, predicted GS/s) for an M-tap filter (host-only, no GPU needed)."""
+    n, g = _I(), ctypes.c_double()
+    _check(lib().fir_os_choose_n(int(M), REAL if real else COMPLEX, int(sms), ctypes.byref(n), ctypes.byref(g)))
+    return n.value, g.value
+
+
+def predict_gsps(M: int, N: int, real: bool = False, sms: int = 0) -> float:
+    """fir_os_predict_gsps: predicted GS/s of an (M, N) plan (host-only)."""
+    g = ctypes.c_double()
+    _check(lib().fir_os_predict_gsps(int(M), int(N), REAL if real else COMPLEX, int(sms), ctypes.byref(g)))
+    return g.value
 
 
 class FirOsError(RuntimeError):

@@ -204,6 +204,21 @@ int fir_os_device_status(fir_os_plan_t plan, void *stream);
 int fir_os_frequency_response_noalloc(const void *h_dev, int M, int N, int h_complex,
                                       void *H_dev, void *stream);
 
+/* fir_os_choose_n -- the FFT size for an M-tap filter: the power of two N in [max(64, M), 65536]
+ * with the highest predicted throughput, and that throughput (output samples per second / 1e9)
+ * in *gsps (may be NULL).  The claim of "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法"
+ * (主权项, 步骤二) leaves N free beyond N = L + M - 1; a longer N spends more transform work per
+ * block on more outputs per block.  The prediction is L x sms / t(N, L/N): t is the device time
+ * of one block in SM-microseconds, measured on a GB300 for every N at L/N = 1/4, 1/2, 3/4 in
+ * large calls and interpolated linearly in L/N.  sms = 0 means the GB300's 152.  Host-only: no
+ * device call.  FIR_OS_E_INVAL for M < 1, a bad data_kind or sms < 0; FIR_OS_E_UNSUPPORTED for
+ * M > 65536. */
+int fir_os_choose_n(int M, int data_kind, int sms, int *N, double *gsps);
+
+/* fir_os_predict_gsps -- the prediction fir_os_choose_n maximises, for one (M, N).  Errors as
+ * fir_os_plan_create's for N and M. */
+int fir_os_predict_gsps(int M, int N, int data_kind, int sms, double *gsps);
+
 /* fir_os_status_string -- a static description of a status code. */
 const char *fir_os_status_string(int status);
 
