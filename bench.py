@@ -375,8 +375,11 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
            "h2d_bytes_per_step": w.channels * (w.n * sb + len(w.calls) * (w.M - 1) * sb),
            "d2h_bytes_per_step": w.channels * (w.n * sb + len(w.calls) * (w.M - 1) * sb),
            "steps": e2e_steps,
-           "path": "fir_os_execute_host on page-locked host buffers: the fused kernel reads x and "
-                   "writes y and the state in host memory in place over the host link"}
+           "path": "fir_os_execute_host on page-locked host buffers: " + (
+               "the fused kernel reads x and writes y and the state in host memory in place over "
+               "the host link" if plan.kernel()["kind"] == "cta" else
+               "chunks of ~2^21 samples copied in and out by the copy engines, pipelined against "
+               "the kernel")}
 
     out = {
         "metric": METRIC, "value": value, "unit": "GS/s", "n_gpus": world, "steps": K,

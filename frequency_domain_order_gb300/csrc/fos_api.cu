@@ -757,11 +757,13 @@ int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n, void 
         return fail(FIR_OS_E_INVAL, "x and y overlap");
     cudaStream_t caller = static_cast<cudaStream_t>(stream_);
 
-    // Page-locked buffers are read and written in place by the kernel over the host link: no
-    // staging copies and no pipeline to fill and drain.  (Measured on this path's host link, this
-    // beats copying x in by the copy engine while the kernel writes y in place.)
+    // With the block kernel, page-locked buffers are read and written in place over the host link:
+    // no staging copies and no pipeline to fill and drain (measured faster than the copy-engine
+    // pipeline below, and than copying x in by the copy engine while the kernel writes y in
+    // place).  The resident and pair kernels go through the copy-engine pipeline: their gather
+    // is point by point, and the pair kernel reads every window twice (once per CTA).
     void *xd = nullptr, *yd = nullptr, *sd = nullptr;
-    if (n > 0 && host_mapped(x_host, &xd) && host_mapped(y_host, &yd) &&
+    if (n > 0 && plan->kernel.split_c == 0 && host_mapped(x_host, &xd) && host_mapped(y_host, &yd) &&
         (plan->M == 1 || host_mapped(state_host, &sd))) {
         if ((reinterpret_cast<uintptr_t>(xd) | reinterpret_cast<uintptr_t>(yd)) & (uintptr_t)(sb - 1) ||
             (plan->M > 1 && (reinterpret_cast<uintptr_t>(sd) & (uintptr_t)(sb - 1))))

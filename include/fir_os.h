@@ -137,8 +137,8 @@ int fir_os_execute_batched(fir_os_plan_t plan, const void *x, int64_t x_stride, 
  *   stream           the caller's stream; work is ordered after it and it is synchronised
  *
  * When x, y and the state are all page-locked (cudaHostAlloc / cudaHostRegister, e.g. torch
- * pin_memory), the kernel reads x and writes y and the state in place over the host link: no
- * staging copies.  Otherwise the call copies chunks of about 2^21 samples (a whole number of
+ * pin_memory) and N <= 8192, the kernel reads x and writes y and the state in place over the
+ * host link: no staging copies.  Otherwise the call copies chunks of about 2^21 samples (a whole number of
  * transforms -- blocks, or block pairs for real data -- so the chunks cut the stream where one
  * fir_os_execute call's transforms begin) through two device buffer sets, pipelined over three
  * streams so that the copies of one chunk overlap the filtering of the next; the plan allocates
