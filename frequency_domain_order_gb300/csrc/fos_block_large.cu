@@ -13,18 +13,4 @@ KernelEntry block_kernel_large(int logn, bool real) {
     }
 }
 
-int pass_twiddle_entries(int logn) {
-    switch (logn) {
-        case 6: return FftShape<6>::TW_ENTRIES;
-        case 7: return FftShape<7>::TW_ENTRIES;
-        case 8: return FftShape<8>::TW_ENTRIES;
-        case 9: return FftShape<9>::TW_ENTRIES;
-        case 10: return FftShape<10>::TW_ENTRIES;
-        case 11: return FftShape<11>::TW_ENTRIES;
-        case 12: return FftShape<12>::TW_ENTRIES;
-        case 13: return FftShape<13>::TW_ENTRIES;
-        default: return 0;
-    }
-}
-
 }  // namespace fos

@@ -69,18 +69,11 @@ struct TwLayout {
 // exchange buffers, so each pass needs one barrier: pass p of the forward transform
 // (INV = false) writes buffer (p mod 2) and reads buffer ((p-1) mod 2); the inverse transform
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
-// transform's last pass reads.  `hook()` runs once, at the start of the last pass, after the
-// barrier that ended the pass before it; the inverse transform's last pass reads only b1, so
-// from there on b0 is free (a caller can start its next copy into it).  Every buffer is
-// xpad_len(N) elements of this transform.
+// transform's last pass reads.  Every buffer is xpad_len(N) elements of this transform.
 
-struct NoHook {
-    __device__ __forceinline__ void operator()() const {}
-};
-
-template <int LOGN, int SMAX, int P, bool INV, class Bar, class Hook>
+template <int LOGN, int SMAX, int P, bool INV, class Bar>
 __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
-                                            uint32_t tm, int j, const Bar &bar, const Hook &hook) {
+                                            uint32_t tm, int j, const Bar &bar) {
     using S = FftShape<LOGN>;
     if constexpr (P < S::NPASS) {
         constexpr int T = S::T;
@@ -88,7 +81,6 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
         constexpr bool last = (P == S::NPASS - 1);
         constexpr int DIR = INV ? 1 : -1;
         constexpr int SH = INV ? S::NPASS + 1 : 0;
-        if constexpr (last) hook();
         float2 *rd = ((P - 1 + SH) % 2 == 0) ? b0 : b1;
         float2 *wr = ((P + SH) % 2 == 0) ? b0 : b1;
         if constexpr (T % 16 == 0) {
@@ -129,16 +121,16 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, SMAX, P + 1, INV>(v, b0, b1, stw, tm, j, bar, hook);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV>(v, b0, b1, stw, tm, j, bar);
     }
 }
 
 // Transform v in place (layout z[j + e T] -> Z[j + e T]).  `bar` synchronises the threads that
 // share the two buffers.  No barrier is needed before the first write: see the buffer rotation
 // above and the callers' barrier placement.
-template <int LOGN, int SMAX, bool INV, class Bar, class Hook = NoHook>
+template <int LOGN, int SMAX, bool INV, class Bar>
 __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
-                                       int j, const Bar &bar, const Hook &hook = Hook()) {
+                                       int j, const Bar &bar) {
     using S = FftShape<LOGN>;
     constexpr int T = S::T, R0 = S::R0, G = 16 / R0;
     constexpr int DIR = INV ? 1 : -1;
@@ -166,7 +158,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, SMAX, 1, INV>(v, b0, b1, stw, tm, j, bar, hook);
+    fft_tm_pass<LOGN, SMAX, 1, INV>(v, b0, b1, stw, tm, j, bar);
 }
 
 }  // namespace fos

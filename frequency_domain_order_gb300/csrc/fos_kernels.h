@@ -82,7 +82,4 @@ KernelEntry resident_kernel(int logn, bool real);
 // One block in the Tensor Memory of a two-CTA cluster, N = 2^16.
 KernelEntry pair_kernel(int logn, bool real);
 
-// Entries of the pass-twiddle table for a per-CTA transform of 2^logn points.
-int pass_twiddle_entries(int logn);
-
 }  // namespace fos
