@@ -16,6 +16,9 @@ claim (主权项):
 * :func:`freq_response`   -- step 1, H = FFT_N(h zero-padded)
 * :func:`overlap_save`    -- steps 2-5 written out block by block (a second, independent
                              CPU formulation used to cross-check :func:`direct`)
+* :func:`channelize`      -- the polyphase channelizer of "GPU加速短波信道化：多相滤波器组的
+                             并行重构与CUDA实现" (a later row built on the same library), as
+                             the defining sum of a K-channel DFT filter bank decimated by D
 
 Pins (tests/test_oracle_pins.py): hand-worked tiny cases, impulse and step responses,
 numpy.convolve and numpy.fft special cases, the complex-exponential eigen-relation,
@@ -84,8 +87,11 @@ class Oracle:
         lib.fo_fft.argtypes = [P, I64, I]
         lib.fo_freq_response.argtypes = [P, I, I64, P]
         lib.fo_overlap_save.argtypes = [P, I64, P, I, I64, P, P]
+        lib.fo_channelize.argtypes = [P, I64, P, I, I, I, P, P]
+        lib.fo_channelize_at.argtypes = [P, I64, P, I, I, I, P, P, I64, P]
         for f in ("fo_direct", "fo_direct_at", "fo_state_next", "fo_dft", "fo_fft",
-                  "fo_freq_response", "fo_overlap_save", "fo_num_threads"):
+                  "fo_freq_response", "fo_overlap_save", "fo_channelize", "fo_channelize_at",
+                  "fo_num_threads"):
             getattr(lib, f).restype = I
         self.lib = lib
         self.path = path
@@ -165,6 +171,37 @@ class Oracle:
                                              _ptr(y)), "overlap_save")
         return y, self.state_next(x, s0, M)
 
+    def channelize(self, x, h, K: int, D: int, state=None):
+        """The K-channel DFT analysis filter bank decimated by D (the channelizer of
+        "GPU加速短波信道化：多相滤波器组的并行重构与CUDA实现"), as its defining sum:
+        y[m, q] = sum_l h[l] e^{-2 pi i q l / K} xt[m D + D - 1 - l].  len(x) must be a
+        multiple of D; state holds len(h) - 1 samples (zeros if None).  Returns
+        (y of shape (len(x) / D, K), complex128; the next state)."""
+        x = _c128(x)
+        h = _c128(h)
+        Nh = h.size
+        s0 = _c128(np.zeros(Nh - 1) if state is None else state)
+        if s0.size != Nh - 1:
+            raise ValueError("state must hold len(h) - 1 samples")
+        if x.size % D:
+            raise ValueError("len(x) must be a multiple of D")
+        y = np.empty((x.size // D, K), dtype=np.complex128)
+        self._check(self.lib.fo_channelize(_ptr(x), x.size, _ptr(h), Nh, K, D, _ptr(s0), _ptr(y)),
+                    "channelize")
+        return y, self.state_next(x, s0, Nh)
+
+    def channelize_at(self, x, h, K: int, D: int, state, ms):
+        """Rows ms of channelize(x, h, K, D, state)[0]."""
+        x = _c128(x)
+        h = _c128(h)
+        Nh = h.size
+        s0 = _c128(np.zeros(Nh - 1) if state is None else state)
+        ms = np.ascontiguousarray(np.asarray(ms, dtype=np.int64))
+        y = np.empty((ms.size, K), dtype=np.complex128)
+        self._check(self.lib.fo_channelize_at(_ptr(x), x.size, _ptr(h), Nh, K, D, _ptr(s0), _ptr(ms),
+                                              ms.size, _ptr(y)), "channelize_at")
+        return y
+
 
 def default() -> Oracle:
     """The oracle built from fir_oracle.c (compiled on first use)."""
@@ -205,3 +242,11 @@ def freq_response(h, N: int):
 
 def overlap_save(x, H, M: int, state=None):
     return default().overlap_save(x, H, M, state)
+
+
+def channelize(x, h, K: int, D: int, state=None):
+    return default().channelize(x, h, K, D, state)
+
+
+def channelize_at(x, h, K: int, D: int, state, ms):
+    return default().channelize_at(x, h, K, D, state, ms)

@@ -19,6 +19,9 @@
  *   fo_fft           iterative radix-2 FFT, same convention as fo_dft
  *   fo_freq_response H = FFT_N(h zero-padded to N)                    (step 1)
  *   fo_overlap_save  steps 2-5 of the claim, written out block by block with fo_fft
+ *   fo_channelize    a K-channel DFT analysis filter bank decimated by D (the polyphase
+ *                    channelizer of "GPU加速短波信道化：多相滤波器组的并行重构与CUDA实现"),
+ *                    written as its defining sum; fo_channelize_at at chosen output times
  *
  * Conventions (the page states neither the DFT sign nor its scaling): the forward
  * transform uses e^{-2 pi i nk/N} unscaled, the inverse e^{+2 pi i nk/N} scaled by 1/N.
@@ -230,6 +233,59 @@ int fo_overlap_save(const double *x, int64_t n, const double *H, int M, int64_t 
         }
     }
     free(E);
+    return 0;
+}
+
+/*
+ * Channelizer.  The page describes the filter bank by its polyphase steps (decimate into
+ * branches, filter each branch with its polyphase component h_k(n) = h(nK + k), DFT across the
+ * branches) with K channels and decimation D = K/2 (50% overlapping channels); those steps
+ * compute the K modulated filters h_q(l) = h(l) e^{-2 pi i q l / K} applied to x and sampled
+ * every D inputs.  The oracle is that definition, not the polyphase algorithm:
+ *
+ *   y[m][q] = sum_{l < Nh} h[l] e^{-2 pi i q l / K} xt[m D + D - 1 - l],   q < K, m < n / D
+ *
+ * Output vector m follows the m-th hop of D new input samples.  xt[t] = x[t] for t >= 0 and
+ * the state S0 (Nh - 1 samples, newest last) for -(Nh-1) <= t < 0.  The angle is reduced
+ * exactly, (q l) mod K, before the cosine and sine.  y is m-major: y[m K + q].
+ */
+static void fo_chan_one(const double *x, int64_t n, const double *h, int Nh, int K, int D, const double *s0,
+                        int64_t m, double *ym) {
+    const int64_t t0 = m * D + D - 1;
+    for (int q = 0; q < K; ++q) {
+        double re = 0.0, im = 0.0;
+        for (int l = 0; l < Nh; ++l) {
+            double a[2];
+            fo_xt(x, n, s0, Nh, t0 - l, &a[0], &a[1]);
+            const int64_t e = ((int64_t)q * l) % K;
+            const double ang = -2.0 * FO_PI * (double)e / (double)K;
+            const double wr = cos(ang), wi = sin(ang);
+            /* h[l] w */
+            const double hr = h[2 * l] * wr - h[2 * l + 1] * wi, hi = h[2 * l] * wi + h[2 * l + 1] * wr;
+            re += hr * a[0] - hi * a[1];
+            im += hr * a[1] + hi * a[0];
+        }
+        ym[2 * q] = re;
+        ym[2 * q + 1] = im;
+    }
+}
+
+int fo_channelize(const double *x, int64_t n, const double *h, int Nh, int K, int D, const double *s0,
+                  double *y) {
+    if (n < 0 || Nh < 1 || K < 1 || D < 1 || n % D != 0) return -1;
+    const int64_t mo = n / D;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < mo; ++m) fo_chan_one(x, n, h, Nh, K, D, s0, m, y + 2 * m * K);
+    return 0;
+}
+
+int fo_channelize_at(const double *x, int64_t n, const double *h, int Nh, int K, int D, const double *s0,
+                     const int64_t *ms, int64_t count, double *y) {
+    if (n < 0 || Nh < 1 || K < 1 || D < 1 || n % D != 0) return -1;
+    for (int64_t i = 0; i < count; ++i)
+        if (ms[i] < 0 || ms[i] >= n / D) return -2;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i) fo_chan_one(x, n, h, Nh, K, D, s0, ms[i], y + 2 * i * K);
     return 0;
 }
 

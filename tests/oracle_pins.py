@@ -202,9 +202,93 @@ def pin_given_response_is_causal(o):
     assert np.abs(he[M:]).max() < 1e-6 * np.abs(h).max()
 
 
+# ----------------------------------------------------------------------------- channelizer
+# The polyphase channelizer of "GPU加速短波信道化：多相滤波器组的并行重构与CUDA实现", read as
+# the K-channel DFT analysis filter bank decimated by D: output vector m follows the m-th hop of
+# D new samples, t_m = m D + D - 1, and channel q is x filtered by h(l) e^{-2 pi i q l / K}.
+
+
+def _folded_response(h, K):
+    """sum_l h[l] e^{-2 pi i r l / K} for r = 0..K-1, through numpy's FFT of the prototype
+    folded modulo K (zero-padded to a multiple of K)."""
+    pad = (-len(h)) % K
+    return np.fft.fft(np.concatenate([h, np.zeros(pad)]).reshape(-1, K).sum(axis=0))
+
+
+def pin_chan_tone(o):
+    """A complex tone at frequency -p0/K that has been running forever (state included) gives
+    every channel q the closed form e^{-2 pi i p0 t_m / K} * Hfold[(q - p0) mod K]."""
+    rng = _rng(31)
+    for K, D, Nh, p0 in [(8, 4, 24, 3), (16, 8, 64, 0), (16, 16, 48, 11), (6, 3, 18, 5)]:
+        h = rng.standard_normal(Nh)
+        n = 10 * D
+        t = np.arange(-(Nh - 1), n)
+        tone = np.exp(-2j * np.pi * p0 * t / K)
+        y, _ = o.channelize(tone[Nh - 1:], h, K, D, tone[:Nh - 1])
+        hf = _folded_response(h, K)
+        tm = np.arange(n // D) * D + D - 1
+        want = np.exp(-2j * np.pi * p0 * tm / K)[:, None] * hf[(np.arange(K) - p0) % K][None, :]
+        assert np.abs(y - want).max() < 1e-11 * np.abs(h).sum(), (K, D, p0)
+
+
+def pin_chan_impulse(o):
+    """x = delta at t0 with zero state: y[m, q] = h[t_m - t0] e^{-2 pi i q (t_m - t0) / K} while
+    0 <= t_m - t0 < Nh, else 0."""
+    rng = _rng(32)
+    K, D, Nh = 8, 2, 40
+    h = rng.standard_normal(Nh)
+    for t0 in (0, 3, 7):
+        n = 40
+        x = np.zeros(n)
+        x[t0] = 1.0
+        y, _ = o.channelize(x, h, K, D)
+        for m in range(n // D):
+            d = m * D + D - 1 - t0
+            want = np.zeros(K, complex)
+            if 0 <= d < Nh:
+                want = h[d] * np.exp(-2j * np.pi * np.arange(K) * d / K)
+            assert np.abs(y[m] - want).max() < 1e-13, (t0, m)
+
+
+def pin_chan_single_channel_is_convolution(o):
+    """K = 1, D = 1 is plain linear convolution with the state in front (numpy.convolve)."""
+    rng = _rng(33)
+    h, x, s0 = _cn(rng, 13), _cn(rng, 50), _cn(rng, 12)
+    y, s1 = o.channelize(x, h, 1, 1, s0)
+    want = np.convolve(np.concatenate([s0, x]), h)[12:12 + 50]
+    assert np.abs(y[:, 0] - want).max() < 1e-12 * np.abs(h).sum()
+    assert np.array_equal(s1, np.concatenate([s0, x])[-12:])
+
+
+def pin_chan_hop_invariant(o):
+    """Decimating by K keeps exactly the odd output vectors of decimating by K/2 (same times)."""
+    rng = _rng(34)
+    K, Nh = 8, 32
+    h, x, s0 = rng.standard_normal(Nh), _cn(rng, 96), _cn(rng, Nh - 1)
+    y1, _ = o.channelize(x, h, K, K, s0)
+    y2, _ = o.channelize(x, h, K, K // 2, s0)
+    assert np.array_equal(y1, y2[1::2])
+
+
+def pin_chan_split_stream(o):
+    """Two calls with the state carried equal one call, exactly; channelize_at picks rows."""
+    rng = _rng(35)
+    K, D, Nh = 16, 8, 48
+    h, x, s0 = rng.standard_normal(Nh), _cn(rng, 160), _cn(rng, Nh - 1)
+    y, s = o.channelize(x, h, K, D, s0)
+    ya, sa = o.channelize(x[:64], h, K, D, s0)
+    yb, sb = o.channelize(x[64:], h, K, D, sa)
+    assert np.array_equal(np.concatenate([ya, yb]), y)
+    assert np.array_equal(sb, s)
+    ms = np.array([0, 5, 19, 3])
+    assert np.array_equal(o.channelize_at(x, h, K, D, s0, ms), y[ms])
+
+
 ALL_PINS = [
     pin_golden_tiny, pin_impulse, pin_step, pin_numpy_convolve, pin_exponential_eigen,
     pin_linearity_and_shift, pin_split_stream, pin_direct_at, pin_dft_textbook,
     pin_fft_library, pin_freq_response, pin_overlap_save_matches_definition,
     pin_given_response_is_causal,
+    pin_chan_tone, pin_chan_impulse, pin_chan_single_channel_is_convolution, pin_chan_hop_invariant,
+    pin_chan_split_stream,
 ]

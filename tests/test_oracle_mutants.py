@@ -43,6 +43,19 @@ MUTANTS = {
     "state carry off by one": (
         "fo_xt(x, n, s0, M, n - (int64_t)(M - 1) + t, &re, &im);",
         "fo_xt(x, n, s0, M, n - (int64_t)M + t, &re, &im);"),
+    "channelizer twiddle sign flipped": (
+        "const double ang = -2.0 * FO_PI * (double)e / (double)K;",
+        "const double ang = 2.0 * FO_PI * (double)e / (double)K;"),
+    "channelizer output at the start of the hop": (
+        "const int64_t t0 = m * D + D - 1;", "const int64_t t0 = m * D;"),
+    "channelizer prototype reversed": (
+        "const double hr = h[2 * l] * wr - h[2 * l + 1] * wi, hi = h[2 * l] * wi + h[2 * l + 1] * wr;",
+        "const double hr = h[2 * (Nh - 1 - l)] * wr - h[2 * (Nh - 1 - l) + 1] * wi, "
+        "hi = h[2 * (Nh - 1 - l)] * wi + h[2 * (Nh - 1 - l) + 1] * wr;"),
+    "channelizer modulation period D instead of K": (
+        "const int64_t e = ((int64_t)q * l) % K;", "const int64_t e = ((int64_t)q * l) % D;"),
+    "channelizer conjugated product": (
+        "im += hr * a[1] + hi * a[0];", "im += hr * a[1] - hi * a[0];"),
     "sampled evaluator shifted": (
         "fo_one(x, n, h, M, s0, idx[q], &y_at[2 * q], &y_at[2 * q + 1]);",
         "fo_one(x, n, h, M, s0, idx[q] + 1, &y_at[2 * q], &y_at[2 * q + 1]);"),
