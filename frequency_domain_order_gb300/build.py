@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfir_os.so")
 
-SOURCES = ["fos_api.cu", "fos_block_small.cu", "fos_block_large.cu", "fos_resident.cu", "fos_pair.cu"]
+SOURCES = ["fos_api.cu", "fos_block_small.cu", "fos_block_large.cu", "fos_resident.cu", "fos_pair.cu", "fos_chan.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

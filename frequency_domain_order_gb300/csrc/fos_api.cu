@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "fir_os.h"  // include/ is on the include path (build.py)
+#include "fos_chan.h"
 #include "fos_fft.cuh"
 #include "fos_kernels.h"
 
@@ -862,6 +863,163 @@ int fir_os_frequency_response_noalloc(const void *h_dev, int M, int N, int h_com
     }
     fos_store_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, static_cast<float2 *>(H_dev), N);
     FOS_CUDA(cudaGetLastError(), "frequency-response kernels");
+    return FIR_OS_OK;
+}
+
+// ------------------------------------------------------------------ channelizer
+
+struct fir_chan_plan {
+    int K = 0, D = 0, Nh = 0, P = 0;
+    int data_kind = FIR_OS_REAL;
+    int device = 0;
+    int smem = 0;
+    int max_ctas = 0;
+    fos::ChanEntry kernel;
+    float *d_h = nullptr;
+    float2 *d_tw = nullptr;
+};
+
+int fir_chan_plan_destroy(fir_chan_plan_t plan) {
+    if (!plan) return FIR_OS_OK;
+    cudaDeviceSynchronize();
+    cudaFree(plan->d_h);
+    cudaFree(plan->d_tw);
+    delete plan;
+    return FIR_OS_OK;
+}
+
+int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_kind, const float *h_dev,
+                         void *stream_) {
+    g_last_error[0] = 0;
+    if (!out) return fail(FIR_OS_E_INVAL, "out is NULL");
+    *out = nullptr;
+    if (K < 64 || K > 4096 || (K & (K - 1)) != 0)
+        return fail(FIR_OS_E_UNSUPPORTED, "K = %d is not a power of two in [64, 4096]", K);
+    if (D < 1 || D > K) return fail(FIR_OS_E_INVAL, "D = %d must be in [1, K = %d]", D, K);
+    if (Nh < 1) return fail(FIR_OS_E_INVAL, "Nh = %d < 1", Nh);
+    if (data_kind != FIR_OS_REAL && data_kind != FIR_OS_COMPLEX)
+        return fail(FIR_OS_E_INVAL, "data_kind %d is neither FIR_OS_REAL nor FIR_OS_COMPLEX", data_kind);
+    if (!h_dev) return fail(FIR_OS_E_INVAL, "h is NULL");
+    if (reinterpret_cast<uintptr_t>(h_dev) & 3) return fail(FIR_OS_E_ALIGN, "h must be 4-byte aligned");
+    const int logk = ilog2i(K);
+    fos::ChanEntry k = fos::chan_kernel(logk, data_kind == FIR_OS_REAL);
+    if (!k.func) return fail(FIR_OS_E_UNSUPPORTED, "no channelizer kernel for K = %d", K);
+    const int P = (Nh + K - 1) / K;
+    const int smem = k.smem_fixed + 4 * P * K;
+    int dev = 0;
+    FOS_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    cudaDeviceProp prop;
+    FOS_CUDA(cudaGetDeviceProperties(&prop, dev), "cudaGetDeviceProperties");
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(FIR_OS_E_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major,
+                    prop.minor);
+    if (smem > (int)prop.sharedMemPerBlockOptin)
+        return fail(FIR_OS_E_UNSUPPORTED, "a prototype of %d taps (%d per branch) does not fit shared memory "
+                                          "with K = %d (at most %d taps)",
+                    Nh, P, K, (int)((prop.sharedMemPerBlockOptin - k.smem_fixed) / (4 * K)) * K);
+    fir_chan_plan *p = new (std::nothrow) fir_chan_plan;
+    if (!p) return fail(FIR_OS_E_NOMEM, "plan allocation failed");
+    auto bail = [&](int status) {
+        fir_chan_plan_destroy(p);
+        return status;
+    };
+    p->K = K;
+    p->D = D;
+    p->Nh = Nh;
+    p->P = P;
+    p->data_kind = data_kind;
+    p->device = dev;
+    p->smem = smem;
+    p->kernel = k;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.func, k.threads, (size_t)smem);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "occupancy query"));
+    if (per_sm < 1) return bail(fail(FIR_OS_E_UNSUPPORTED, "channelizer kernel does not fit an SM"));
+    p->max_ctas = per_sm * prop.multiProcessorCount;
+    std::vector<float2> tw;
+    if (!pass_twiddles(logk, tw)) return bail(fail(FIR_OS_E_UNSUPPORTED, "twiddles"));
+    if ((e = cudaMalloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess ||
+        (e = cudaMalloc(&p->d_h, sizeof(float) * Nh)) != cudaSuccess)
+        return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc failed"));
+    if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice, stream)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(p->d_h, h_dev, sizeof(float) * Nh, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+        return bail(cuda_fail(e, "plan upload"));
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));
+    *out = p;
+    return FIR_OS_OK;
+}
+
+int fir_chan_plan_info(fir_chan_plan_t plan, int *K, int *D, int *Nh) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (K) *K = plan->K;
+    if (D) *D = plan->D;
+    if (Nh) *Nh = plan->Nh;
+    return FIR_OS_OK;
+}
+
+int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n, void *y, void *state, void *stream_) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (n < 0) return fail(FIR_OS_E_INVAL, "n_samples < 0");
+    if (n % plan->D) return fail(FIR_OS_E_INVAL, "n_samples = %lld is not a multiple of D = %d", (long long)n, plan->D);
+    if (n == 0) return FIR_OS_OK;
+    const int sb = plan->data_kind == FIR_OS_REAL ? 4 : 8;
+    const int hist = plan->Nh - 1;
+    if (!x || !y) return fail(FIR_OS_E_INVAL, "x or y is NULL");
+    if (hist > 0 && !state) return fail(FIR_OS_E_INVAL, "state is NULL but Nh > 1");
+    const uintptr_t ux = reinterpret_cast<uintptr_t>(x), uy = reinterpret_cast<uintptr_t>(y),
+                    us = reinterpret_cast<uintptr_t>(state);
+    if ((ux & (uintptr_t)(sb - 1)) || (uy & 7) || (hist > 0 && (us & (uintptr_t)(sb - 1))))
+        return fail(FIR_OS_E_ALIGN, "x and the state must be %d-byte aligned, y 8-byte aligned", sb);
+    const int64_t nout = n / plan->D;
+    const size_t xb = (size_t)n * sb, yb = (size_t)nout * plan->K * 8, stb = (size_t)hist * sb;
+    if (ranges_overlap(ux, xb, uy, yb)) return fail(FIR_OS_E_INVAL, "x and y overlap");
+    if (ranges_overlap(us, stb, ux, xb) || ranges_overlap(us, stb, uy, yb))
+        return fail(FIR_OS_E_INVAL, "state overlaps x or y");
+    int dev = -1;
+    FOS_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != plan->device)
+        return fail(FIR_OS_E_INVAL, "plan was created on device %d but device %d is current", plan->device, dev);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    fos::ChanParams cp{};
+    cp.x = x;
+    cp.y = static_cast<float2 *>(y);
+    cp.state = state;
+    cp.h = plan->d_h;
+    cp.tw = plan->d_tw;
+    cp.nout = nout;
+    cp.nunits = (nout + plan->kernel.per_unit - 1) / plan->kernel.per_unit;
+    cp.K = plan->K;
+    cp.D = plan->D;
+    cp.Nh = plan->Nh;
+    cp.P = plan->P;
+    const int64_t want = (cp.nunits + plan->kernel.groups - 1) / plan->kernel.groups;
+    const int64_t grid = want < plan->max_ctas ? want : plan->max_ctas;
+    void *args[] = {&cp};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(plan->kernel.threads);
+    cfg.dynamicSmemBytes = (size_t)plan->smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    FOS_CUDA(cudaLaunchKernelExC(&cfg, plan->kernel.func, args), "channelizer launch");
+    if (hist > 0) {
+        // S0' = the last Nh - 1 samples of concat(S0, x), after the filter bank has read S0
+        if (plan->data_kind == FIR_OS_REAL)
+            fos_state_kernel<float><<<1, 1024, 0, stream>>>(static_cast<const float *>(x), n,
+                                                            static_cast<float *>(state), hist, 0, 0);
+        else
+            fos_state_kernel<float2><<<1, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
+                                                             static_cast<float2 *>(state), hist, 0, 0);
+        FOS_CUDA(cudaGetLastError(), "state kernel launch");
+    }
     return FIR_OS_OK;
 }
 

@@ -1,0 +1,142 @@
+// fos_chan.cu -- the polyphase DFT channelizer of "GPU加速短波信道化：多相滤波器组的并行重构与
+// CUDA实现": a K-channel analysis filter bank decimated by D,
+//
+//   y[m][q] = sum_{l < Nh} h[l] e^{-2 pi i q l / K} xt[t_m - l],   t_m = m D + D - 1,
+//
+// computed as the page's three steps: the input is dealt into K branches (branch k of output
+// m reads xt[t_m - k - r K], r = 0, 1, ...), each branch is filtered by its polyphase component
+// h_k(r) = h[r K + k], and a K-point DFT across the branches gives the K channels:
+//
+//   v_k(m) = sum_r h[r K + k] xt[t_m - r K - k],   y[m][q] = sum_k v_k(m) e^{-2 pi i q k / K}.
+//
+// Thread j of a transform computes v_k for k = j + (K/16) e, e = 0..15 -- exactly the register
+// layout of the K-point Stockham FFT of fos_fft.cuh, which then runs with its twiddles in
+// shared memory (no Tensor Memory: the prototype, not per-thread constants, fills shared
+// memory).  A group of max(64, K/16) threads transforms F = max(1, 64 / (K/16)) consecutive
+// output vectors; a CTA of 512 threads holds 512 / group groups, each with two exchange
+// buffers per transform; the (zero-padded) prototype h[r K + k] lives once per CTA in shared
+// memory.  Grid: persistent, one CTA per SM, units of F output vectors round-robin over all
+// groups.  The input is read through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
+#include <type_traits>
+
+#include "fos_chan.h"
+#include "fos_fft.cuh"
+
+namespace fos {
+
+template <int LOGK, bool REAL>
+struct ChanCfg {
+    using S = FftShape<LOGK>;
+    static constexpr int K = S::N;
+    static constexpr int T = S::T;                // threads of one transform
+    static constexpr int F = T >= 64 ? 1 : 64 / T;
+    static constexpr int GT = F * T;              // threads of one group
+    static constexpr int THREADS = 512;
+    static constexpr int GROUPS = THREADS / GT;
+    using TL = TwLayout<LOGK, (1 << 30)>;         // every pass twiddle in shared memory
+    static constexpr int EX = xpad_len(K);        // elements of one exchange buffer
+    static constexpr int OFF_TW = 0;
+    static constexpr int OFF_BUF = (8 * TL::SMEM_ENTRIES + 127) / 128 * 128;
+    static constexpr int OFF_H = OFF_BUF + GROUPS * F * 2 * 8 * EX;  // then P K floats of h
+    static constexpr int smem_bytes(int P) { return OFF_H + 4 * P * K; }
+    using Bar = GroupBarrier<GT>;
+};
+
+template <int LOGK, bool REAL>
+__global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
+    using C = ChanCfg<LOGK, REAL>;
+    using T_ = typename std::conditional<REAL, float, float2>::type;
+    constexpr int K = C::K, T = C::T;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x;
+    const int g = tid / C::GT, tg = tid % C::GT;
+    const int f = tg / T, j = tg % T;
+    float2 *stw = reinterpret_cast<float2 *>(smem + C::OFF_TW);
+    float2 *b0 = reinterpret_cast<float2 *>(smem + C::OFF_BUF) + (g * C::F + f) * 2 * C::EX;
+    float2 *b1 = b0 + C::EX;
+    float *hs = reinterpret_cast<float *>(smem + C::OFF_H);
+    const typename C::Bar gbar{1 + g};
+
+    griddep_launch_dependents();  // the next call's kernel may start its own set-up
+    for (int i = tid; i < C::TL::SMEM_ENTRIES; i += C::THREADS) stw[i] = p.tw[i];
+    for (int i = tid; i < p.P * K; i += C::THREADS) hs[i] = i < p.Nh ? p.h[i] : 0.f;
+    __syncthreads();
+    // the set-up read plan memory only; x, y and the state may belong to the previous kernel
+    griddep_wait();
+
+    const T_ *x = static_cast<const T_ *>(p.x);
+    const T_ *s0 = static_cast<const T_ *>(p.state);
+    float2 *y = p.y;
+    const int64_t hist = p.Nh - 1;
+    const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
+    for (int64_t u = (int64_t)blockIdx.x * C::GROUPS + g; u < p.nunits; u += stride) {
+        const int64_t m = u * C::F + f;
+        const bool live = m < p.nout;  // a partial last unit: the spare transforms idle
+        const int64_t tm = m * p.D + p.D - 1;
+        float2 v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
+        if (live) {
+            // branch sums: v[e] = v_k(m), k = j + T e
+            const bool interior = tm - (int64_t)p.P * K + 1 >= 0;  // no branch reaches the state
+#pragma unroll 1
+            for (int r = 0; r < p.P; ++r) {
+                const int64_t tb = tm - (int64_t)r * K - j;
+                float hr[16];
+                T_ xv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    hr[e] = hs[r * K + j + T * e];
+                    const int64_t t = tb - T * e;
+                    if (interior || t >= 0) xv[e] = x[t];
+                    else xv[e] = t >= -hist ? s0[hist + t] : T_{};
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    if constexpr (REAL) {
+                        v[e].x = fmaf(hr[e], xv[e], v[e].x);
+                    } else {
+                        v[e].x = fmaf(hr[e], xv[e].x, v[e].x);
+                        v[e].y = fmaf(hr[e], xv[e].y, v[e].y);
+                    }
+                }
+            }
+        }
+        // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
+        fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
+        if (live) {
+            float2 *ym = y + m * K + j;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) st_cs(ym + T * e, v[e]);
+        }
+        gbar.sync();  // the next unit's first pass may write the buffer this one's last pass read
+    }
+}
+
+template <int LOGK, bool REAL>
+ChanEntry chan_entry() {
+    using C = ChanCfg<LOGK, REAL>;
+    ChanEntry k;
+    k.func = reinterpret_cast<const void *>(&fos_chan_kernel<LOGK, REAL>);
+    k.threads = C::THREADS;
+    k.groups = C::GROUPS;
+    k.per_unit = C::F;
+    k.smem_fixed = C::OFF_H;
+    k.tw_entries = C::TL::SMEM_ENTRIES;
+    return k;
+}
+
+ChanEntry chan_kernel(int logk, bool real) {
+    switch (logk) {
+        case 6: return real ? chan_entry<6, true>() : chan_entry<6, false>();
+        case 7: return real ? chan_entry<7, true>() : chan_entry<7, false>();
+        case 8: return real ? chan_entry<8, true>() : chan_entry<8, false>();
+        case 9: return real ? chan_entry<9, true>() : chan_entry<9, false>();
+        case 10: return real ? chan_entry<10, true>() : chan_entry<10, false>();
+        case 11: return real ? chan_entry<11, true>() : chan_entry<11, false>();
+        case 12: return real ? chan_entry<12, true>() : chan_entry<12, false>();
+        default: return ChanEntry{};
+    }
+}
+
+}  // namespace fos

@@ -45,6 +45,10 @@ SIGNATURES = {
     "fir_os_frequency_response_noalloc": (_I, [_P, _I, _I, _I, _P, _P]),
     "fir_os_choose_n": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
     "fir_os_predict_gsps": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_double)]),
+    "fir_chan_plan_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _P, _P]),
+    "fir_chan_execute": (_I, [_P, _P, _I64, _P, _P, _P]),
+    "fir_chan_plan_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "fir_chan_plan_destroy": (_I, [_P]),
     "fir_os_status_string": (ctypes.c_char_p, [_I]),
     "fir_os_last_error": (ctypes.c_char_p, []),
 }
@@ -209,3 +213,32 @@ class Plan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class ChanPlan:
+    """A polyphase DFT channelizer (fir_chan_plan_*): K channels of the prototype h, decimated
+    by D.  h is a CUDA float32 tensor of Nh taps."""
+
+    def __init__(self, K: int, D: int, h, real: bool = True, stream=None):
+        hp = _P()
+        _check(lib().fir_chan_plan_create(ctypes.byref(hp), int(K), int(D), int(h.numel()),
+                                          REAL if real else COMPLEX, h.data_ptr(), _stream_handle(stream)))
+        self._h = hp
+        self.K, self.D, self.Nh, self.real = int(K), int(D), int(h.numel()), real
+
+    def execute(self, x, y, state, stream=None):
+        """fir_chan_execute on CUDA tensors: x (n,), y (n / D, K) complex64, state (Nh - 1,)."""
+        _check(lib().fir_chan_execute(self._h, x.data_ptr(), int(x.numel()), y.data_ptr(), _ptr(state),
+                                      _stream_handle(stream)))
+        return y
+
+    def close(self):
+        if self._h:
+            lib().fir_chan_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

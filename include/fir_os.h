@@ -57,6 +57,7 @@ extern "C" {
 #define FIR_OS_COEF_FREQ 1 /* coef = H, N bins of complex64 (step 1, second case) */
 
 typedef struct fir_os_plan *fir_os_plan_t;
+typedef struct fir_chan_plan *fir_chan_plan_t;
 
 /*
  * fir_os_plan_create -- step 1: build the frequency response and everything the block
@@ -218,6 +219,44 @@ int fir_os_choose_n(int M, int data_kind, int sms, int *N, double *gsps);
 /* fir_os_predict_gsps -- the prediction fir_os_choose_n maximises, for one (M, N).  Errors as
  * fir_os_plan_create's for N and M. */
 int fir_os_predict_gsps(int M, int N, int data_kind, int sms, double *gsps);
+
+/* ---------------------------------------------------------------------------------------
+ * Polyphase DFT channelizer ("GPU加速短波信道化：多相滤波器组的并行重构与CUDA实现", sections 2-3):
+ * K channels of a real lowpass prototype h (Nh taps) modulated to the K frequencies q / K and
+ * decimated by D (D = K/2 for the page's 50%-overlapping channels),
+ *
+ *   y[m][q] = sum_{l < Nh} h[l] e^{-2 pi i q l / K} xt[m D + D - 1 - l],
+ *
+ * computed by the page's three steps: input dealt into K branches, each branch filtered by its
+ * polyphase component h[r K + k], a K-point DFT across the branches.  xt is x preceded by the
+ * state (Nh - 1 samples, oldest first, carried from call to call like fir_os_execute's).
+ */
+
+/* fir_chan_plan_create -- K a power of two in [64, 4096]; 1 <= D <= K; Nh >= 1 with
+ * ceil(Nh / K) K taps fitting shared memory (FIR_OS_E_UNSUPPORTED otherwise; the message gives
+ * the limit, 20 K taps at K = 1024); data_kind FIR_OS_REAL (float32 x) or FIR_OS_COMPLEX
+ * (complex64 x); h_dev: Nh float32 taps in device memory, 4-byte aligned, copied into the plan
+ * (the call synchronises `stream`, so h_dev may be freed afterwards).  Errors as
+ * fir_os_plan_create's. */
+int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_kind, const float *h_dev,
+                         void *stream);
+
+/* fir_chan_execute -- one call over n_samples input samples, asynchronous on `stream`.
+ *   x       device memory, n_samples samples (float32 or complex64), naturally aligned
+ *   y       device memory, (n_samples / D) x K complex64 outputs, y[m K + q], 8-byte aligned
+ *   state   device memory, Nh - 1 samples in/out (NULL only if Nh == 1); zero it before the
+ *           first call of a stream
+ * n_samples must be a multiple of D (FIR_OS_E_INVAL otherwise); 0 is a no-op.  x, y and the
+ * state must not overlap (FIR_OS_E_INVAL).  Launches the channelizer kernel and, when Nh > 1,
+ * a one-CTA kernel that writes the new state. */
+int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n_samples, void *y, void *state,
+                     void *stream);
+
+/* fir_chan_plan_info -- K, D and Nh of a channelizer plan (any output may be NULL). */
+int fir_chan_plan_info(fir_chan_plan_t plan, int *K, int *D, int *Nh);
+
+/* fir_chan_plan_destroy -- synchronises the device and frees the plan.  NULL is a no-op. */
+int fir_chan_plan_destroy(fir_chan_plan_t plan);
 
 /* fir_os_status_string -- a static description of a status code. */
 const char *fir_os_status_string(int status);

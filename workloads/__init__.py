@@ -300,3 +300,55 @@ def errors(got: np.ndarray, want: np.ndarray):
     rel = float(np.linalg.norm(d)) / den if den > 0 else float(np.linalg.norm(d))
     mx = float(np.max(np.abs(d))) if d.size else 0.0
     return rel, mx
+
+
+# ----------------------------------------------------------------------------- channelizer
+# The polyphase channelizer of "GPU加速短波信道化：多相滤波器组的并行重构与CUDA实现": input of
+# 262144 = 2^18 float32 samples (40 ms at 6.5536 MHz); K = 128 or 1024 channels decimated by
+# D = K/2 (50% overlapping channels); a Hamming-windowed lowpass prototype with cutoff 1/D of
+# Nyquist (the page's firwin(Nh, 1/D, fs=2) design).  The page's prototype lengths (100 and 50
+# taps) are shorter than K, which its own text flags as an error; the reading here is 8 taps per
+# branch, Nh = 8 K.  Input: real N(0,1), seeded.
+
+
+@dataclasses.dataclass(frozen=True)
+class Channelizer:
+    name: str
+    K: int                # channels
+    D: int                # decimation
+    Nh: int               # prototype taps
+    n: int                # input samples (a multiple of D)
+    real: bool
+    x_seed: int
+    description: str = ""
+
+    @property
+    def nout(self) -> int:
+        return self.n // self.D
+
+    @property
+    def sample_bytes(self) -> int:
+        return 4 if self.real else 8
+
+
+CHANNELIZERS = {
+    "P1": Channelizer("P1", 128, 64, 1024, 1 << 18, True, 40,
+                      "128 channels, D=64, Nh=1024 Hamming lowpass 1/64, 2^18 real samples"),
+    "P2": Channelizer("P2", 1024, 512, 8192, 1 << 18, True, 41,
+                      "1024 channels, D=512, Nh=8192 Hamming lowpass 1/512, 2^18 real samples"),
+    "P2big": Channelizer("P2big", 1024, 512, 8192, 1 << 26, True, 42,
+                         "1024 channels, D=512, Nh=8192 Hamming lowpass 1/512, 2^26 real samples"),
+}
+
+
+def chan_prototype(c: Channelizer) -> np.ndarray:
+    """The prototype lowpass (float64): Hamming-windowed sinc, cutoff 1/D of Nyquist, unit DC gain."""
+    return lowpass(c.Nh, 1.0 / c.D, hamming(c.Nh))
+
+
+def chan_x(c: Channelizer) -> np.ndarray:
+    """The input stream: real N(0,1) (float32) or complex N(0,1) (complex64)."""
+    if c.real:
+        rng = np.random.Generator(np.random.PCG64(c.x_seed))
+        return rng.standard_normal(c.n).astype(np.float32)
+    return complex_normal(c.n, c.x_seed).astype(np.complex64)
