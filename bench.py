@@ -489,6 +489,189 @@ def run_reference(args, w: W.Workload, world: int, rank: int):
     }
 
 
+# ----------------------------------------------------------------------------- channelizer
+
+CHAN_METRIC = "polyphase channelizer input GS/s on 1 GB300; % of HBM roofline"
+
+
+def chan_bytes_per_input(c) -> float:
+    """Input read once, K complex64 outputs written per D inputs (prototype and state ignored)."""
+    return c.sample_bytes + 8.0 * c.K / c.D
+
+
+def chan_flops_per_input(c) -> float:
+    """Nominal: the polyphase sums (2 Nh real, 4 Nh complex flops per output vector) and a
+    K-point FFT (5 K log2 K) per output vector, per input sample."""
+    return ((2 if c.real else 4) * c.Nh + 5.0 * c.K * math.log2(c.K)) / c.D
+
+
+def run_chan(args, c, world: int, rank: int, local: int):
+    import torch
+
+    from frequency_domain_order_gb300 import build as fbuild
+    from frequency_domain_order_gb300 import fir_os
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or not os.path.exists(fbuild.LIB):
+        fbuild.build()
+    barrier(world)
+    h = W.chan_prototype(c)
+    x = W.chan_x(c)
+    plan = fir_os.ChanPlan(c.K, c.D, torch.from_numpy(h.astype(np.float32)).to(dev), real=c.real)
+    sets = 2
+    xs = [torch.from_numpy(x).to(dev) for _ in range(sets)]
+    ys = [torch.empty((c.nout, c.K), dtype=torch.complex64, device=dev) for _ in range(sets)]
+    sts = [torch.zeros(c.Nh - 1, dtype=xs[0].dtype, device=dev) for _ in range(sets)]
+    footprint = sets * (x.nbytes + c.nout * c.K * 8)
+    stream = torch.cuda.current_stream(dev)
+    for k in range(sets):
+        plan.execute(xs[k], ys[k], sts[k], stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for k in range(sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.execute(xs[k], ys[k], sts[k], torch.cuda.current_stream(dev))
+        graphs.append(g)
+    for i in range(args.warmup):
+        graphs[i % sets].replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for i in range(K):
+            ev[i][0].record(stream)
+            graphs[i % sets].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    launch_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    ms_step = reduce_max(total_ms / K, world, dev)
+    value = world * c.n / (ms_step * 1e-3) / 1e9
+    peak, peak_kind, peaks = measured_peaks()
+    bytes_step = c.n * chan_bytes_per_input(c)
+    achieved = bytes_step / (launch_ms * 1e-3) / 1e9
+    clk = clocks.summary()
+    sm_mhz = clk["sm_mhz"] if clk else (peaks.get("sm_max_mhz") or 2070.0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    flops_step = c.n * chan_flops_per_input(c)
+    t_hbm = bytes_step / (peak * 1e9)
+    t_fp32 = flops_step / (fp32_peak * 1e12)
+    traffic, _ = profiled_traffic(c.name)
+
+    # end to end: pinned input copied in, the call, the output copied back, every step
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.empty((c.nout, c.K), dtype=torch.complex64).pin_memory()
+
+    def e2e_step():
+        xs[0].copy_(xh, non_blocking=True)
+        plan.execute(xs[0], ys[0], sts[0], stream)
+        yh.copy_(ys[0], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, world, dev)
+    out = {
+        "metric": CHAN_METRIC, "value": value, "unit": "GS/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{c.name}: {c.description}", "n_samples": c.n, "K": c.K, "D": c.D,
+                   "Nh": c.Nh, "sample": "float32" if c.real else "complex64",
+                   "l2": f"steps alternate between 2 input/output buffer sets, {footprint / 1e6:.0f} MB in total "
+                         f"vs {L2_BYTES / 2**20:.0f} MiB L2",
+                   "parallelism": f"{world} GPUs, each its own copy of the stream" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": bytes_step, "kernel_ms_per_launch": launch_ms},
+        "fp32": {"nominal_flops_per_input": chan_flops_per_input(c),
+                 "achieved_tflops": flops_step / (launch_ms * 1e-3) / 1e12, "peak_tflops": fp32_peak,
+                 "frac": flops_step / (launch_ms * 1e-3) / 1e12 / fp32_peak},
+        "metric_roofline": {"t_hbm_us": t_hbm * 1e6, "t_fp32_us": t_fp32 * 1e6,
+                            "bound": "hbm" if t_hbm >= t_fp32 else "fp32",
+                            "frac": max(t_hbm, t_fp32) / (ms_step * 1e-3)},
+        "e2e": {"value": world * c.n / e2e_s / 1e9, "unit": "GS/s",
+                "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": c.nout * c.K * 8, "steps": e2e_steps,
+                "path": "pinned input copied in, fir_chan_execute, output copied back"},
+        "gpu_launches": K * (2 if c.Nh > 1 else 1),
+        "launch_mode": "CUDA graph of the call, replayed",
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        h32 = h.astype(np.float32).astype(np.float64)
+        probe = min(c.nout, 16)
+        t0 = time.perf_counter()
+        oracle.channelize_at(x, h32, c.K, c.D, None, np.arange(probe))
+        rate = probe / max(time.perf_counter() - t0, 1e-6)
+        rows = int(max(1, min(c.nout, rate * args.cpu_budget)))
+        t0 = time.perf_counter()
+        oracle.channelize_at(x, h32, c.K, c.D, None, np.arange(rows))
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": rows * c.D / dt / 1e9, "unit": "GS/s", "cores": oracle.num_threads(),
+                               "kind": "oracle", "seconds": dt,
+                               "sample": f"first {rows} of {c.nout} output vectors ({rows * c.D} input samples), "
+                                         f"float64 defining sum, OpenMP over output vectors"}
+    plan.close()
+    return out
+
+
+def run_chan_reference(args, c, world: int, rank: int):
+    """The oracle as the reference arm on a channelizer workload: each step evaluates a bounded
+    run of output vectors at a seeded offset."""
+    if rank != 0:
+        return None
+    import oracle
+    h = W.chan_prototype(c).astype(np.float32).astype(np.float64)
+    x = W.chan_x(c)
+    probe = min(c.nout, 16)
+    t0 = time.perf_counter()
+    oracle.channelize_at(x, h, c.K, c.D, None, np.arange(probe))
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = min(0.5, 120.0 / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(c.nout, rate * per_step_s)))
+    rng = np.random.Generator(np.random.PCG64(98))
+    starts = rng.integers(0, max(1, c.nout - rows), args.steps + args.warmup)
+    for i in range(args.warmup):
+        oracle.channelize_at(x, h, c.K, c.D, None, np.arange(starts[i], starts[i] + rows))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s0 = starts[args.warmup + i]
+        oracle.channelize_at(x, h, c.K, c.D, None, np.arange(s0, s0 + rows))
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows * c.D / dt / 1e9
+    sample = f"{rows} output vectors per step at seeded offsets ({rows * c.D} input samples), float64 defining sum"
+    return {
+        "metric": CHAN_METRIC, "value": value, "unit": "GS/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{c.name}: {c.description}", "n_samples": c.n, "K": c.K, "D": c.D, "Nh": c.Nh},
+        "cpu_baseline": {"value": value, "unit": "GS/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GS/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 # ----------------------------------------------------------------------------- main
 
 
@@ -498,7 +681,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS) + sorted(W.CHANNELIZERS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--direct", action="store_true",
@@ -510,11 +693,16 @@ def main(argv=None):
     world, rank, local = dist_setup()
     if world != args.gpus:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
-    w = W.WORKLOADS[args.config]
-    if args.impl == "reference":
-        out = run_reference(args, w, world, rank)
+    if args.config in W.CHANNELIZERS:
+        c = W.CHANNELIZERS[args.config]
+        out = run_chan_reference(args, c, world, rank) if args.impl == "reference" else run_chan(
+            args, c, world, rank, local)
     else:
-        out = run_ours(args, w, world, rank, local)
+        w = W.WORKLOADS[args.config]
+        if args.impl == "reference":
+            out = run_reference(args, w, world, rank)
+        else:
+            out = run_ours(args, w, world, rank, local)
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     if world > 1 and args.impl == "ours":

@@ -42,6 +42,36 @@ struct ChanCfg {
     using Bar = GroupBarrier<GT>;
 };
 
+// v[e] += sum over taps r0 .. r0 + NR - 1 of h[r K + k] xt[t_m - r K - k], k = j + T e: all
+// 16 NR loads of x are issued before the first multiply-add.
+template <int NR, int K, int T, bool REAL, typename T_>
+__device__ __forceinline__ void branch_taps(float2 (&v)[16], const float *hs, const T_ *x, const T_ *s0,
+                                            int64_t hist, int64_t tm, int r0, int j, bool interior) {
+    T_ xv[NR][16];
+#pragma unroll
+    for (int q = 0; q < NR; ++q) {
+        const int64_t tb = tm - (int64_t)(r0 + q) * K - j;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int64_t t = tb - T * e;
+            if (interior || t >= 0) xv[q][e] = x[t];
+            else xv[q][e] = t >= -hist ? s0[hist + t] : T_{};
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NR; ++q)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float hr = hs[(r0 + q) * K + j + T * e];
+            if constexpr (REAL) {
+                v[e].x = fmaf(hr, xv[q][e], v[e].x);
+            } else {
+                v[e].x = fmaf(hr, xv[q][e].x, v[e].x);
+                v[e].y = fmaf(hr, xv[q][e].y, v[e].y);
+            }
+        }
+}
+
 template <int LOGK, bool REAL>
 __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     using C = ChanCfg<LOGK, REAL>;
@@ -77,30 +107,15 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
         if (live) {
-            // branch sums: v[e] = v_k(m), k = j + T e
+            // branch sums: v[e] = v_k(m), k = j + T e; several taps of every branch in flight at a
+            // time (four for real input, two for complex), then one tap at a time
+            constexpr int NR = REAL ? 4 : 2;
             const bool interior = tm - (int64_t)p.P * K + 1 >= 0;  // no branch reaches the state
+            int r = 0;
 #pragma unroll 1
-            for (int r = 0; r < p.P; ++r) {
-                const int64_t tb = tm - (int64_t)r * K - j;
-                float hr[16];
-                T_ xv[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    hr[e] = hs[r * K + j + T * e];
-                    const int64_t t = tb - T * e;
-                    if (interior || t >= 0) xv[e] = x[t];
-                    else xv[e] = t >= -hist ? s0[hist + t] : T_{};
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    if constexpr (REAL) {
-                        v[e].x = fmaf(hr[e], xv[e], v[e].x);
-                    } else {
-                        v[e].x = fmaf(hr[e], xv[e].x, v[e].x);
-                        v[e].y = fmaf(hr[e], xv[e].y, v[e].y);
-                    }
-                }
-            }
+            for (; r + NR <= p.P; r += NR) branch_taps<NR, K, T, REAL>(v, hs, x, s0, hist, tm, r, j, interior);
+#pragma unroll 1
+            for (; r < p.P; ++r) branch_taps<1, K, T, REAL>(v, hs, x, s0, hist, tm, r, j, interior);
         }
         // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
         fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
