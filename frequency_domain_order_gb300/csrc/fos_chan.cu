@@ -43,26 +43,37 @@ struct ChanCfg {
 };
 
 // v[e] += sum over taps r0 .. r0 + NR - 1 of h[r K + k] xt[t_m - r K - k], k = j + T e: all
-// 16 NR loads of x are issued before the first multiply-add.
-template <int NR, int K, int T, bool REAL, typename T_>
+// 16 NR loads of x are issued before the first multiply-add.  INTERIOR: every index is inside
+// x, so the loads are one base pointer with constant offsets through the read-only path;
+// otherwise each index is checked and the state (or zero) read in front of x.
+template <int NR, int K, int T, bool REAL, bool INTERIOR, typename T_>
 __device__ __forceinline__ void branch_taps(float2 (&v)[16], const float *hs, const T_ *x, const T_ *s0,
-                                            int64_t hist, int64_t tm, int r0, int j, bool interior) {
+                                            int64_t hist, int64_t tm, int r0, int j) {
     T_ xv[NR][16];
+    if constexpr (INTERIOR) {
+        const T_ *xb = x + (tm - (int64_t)r0 * K - j);
 #pragma unroll
-    for (int q = 0; q < NR; ++q) {
-        const int64_t tb = tm - (int64_t)(r0 + q) * K - j;
+        for (int q = 0; q < NR; ++q)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int64_t t = tb - T * e;
-            if (interior || t >= 0) xv[q][e] = x[t];
-            else xv[q][e] = t >= -hist ? s0[hist + t] : T_{};
+            for (int e = 0; e < 16; ++e) xv[q][e] = __ldg(xb - (q * K + T * e));
+    } else {
+#pragma unroll
+        for (int q = 0; q < NR; ++q) {
+            const int64_t tb = tm - (int64_t)(r0 + q) * K - j;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int64_t t = tb - T * e;
+                if (t >= 0) xv[q][e] = x[t];
+                else xv[q][e] = t >= -hist ? s0[hist + t] : T_{};
+            }
         }
     }
+    const float *hb = hs + r0 * K + j;
 #pragma unroll
     for (int q = 0; q < NR; ++q)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            const float hr = hs[(r0 + q) * K + j + T * e];
+            const float hr = hb[q * K + T * e];
             if constexpr (REAL) {
                 v[e].x = fmaf(hr, xv[q][e], v[e].x);
             } else {
@@ -110,12 +121,16 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
             // branch sums: v[e] = v_k(m), k = j + T e; several taps of every branch in flight at a
             // time (four for real input, two for complex), then one tap at a time
             constexpr int NR = REAL ? 4 : 2;
-            const bool interior = tm - (int64_t)p.P * K + 1 >= 0;  // no branch reaches the state
             int r = 0;
+            if (tm - (int64_t)p.P * K + 1 >= 0) {  // no branch reaches the state
 #pragma unroll 1
-            for (; r + NR <= p.P; r += NR) branch_taps<NR, K, T, REAL>(v, hs, x, s0, hist, tm, r, j, interior);
+                for (; r + NR <= p.P; r += NR) branch_taps<NR, K, T, REAL, true>(v, hs, x, s0, hist, tm, r, j);
 #pragma unroll 1
-            for (; r < p.P; ++r) branch_taps<1, K, T, REAL>(v, hs, x, s0, hist, tm, r, j, interior);
+                for (; r < p.P; ++r) branch_taps<1, K, T, REAL, true>(v, hs, x, s0, hist, tm, r, j);
+            } else {
+#pragma unroll 1
+                for (; r < p.P; ++r) branch_taps<1, K, T, REAL, false>(v, hs, x, s0, hist, tm, r, j);
+            }
         }
         // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
         fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
