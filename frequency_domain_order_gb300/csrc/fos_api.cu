@@ -294,9 +294,9 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.L = p->L;
     bp.fuse_state = fuse_state(p, n);
     bp.no_bulk = host_resident ? 1 : 0;
-    // CTAs (or clusters) to launch: enough groups for every unit, at most what is resident
-    const int64_t want = (bp.nunits + p->kernel.groups - 1) / p->kernel.groups;
-    const int64_t groups = want < p->max_units_in_flight ? want : p->max_units_in_flight;
+    // CTAs (or clusters) to launch: one per unit, at most what is resident, so that a call of
+    // few units runs on as many SMs as it can (the block kernel deals units across CTAs first)
+    const int64_t groups = bp.nunits < p->max_units_in_flight ? bp.nunits : p->max_units_in_flight;
     void *args[] = {&bp};
     // programmatic serialization: the kernel's set-up (Tensor Memory, plan constants) overlaps
     // the end of the kernel before it in the stream; it waits for that kernel before it touches
@@ -991,13 +991,19 @@ int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n, void *y, vo
     cp.h = plan->d_h;
     cp.tw = plan->d_tw;
     cp.nout = nout;
-    cp.nunits = (nout + plan->kernel.per_unit - 1) / plan->kernel.per_unit;
+    // real input shares a transform between two output vectors when the call fills every
+    // group of the device at least twice over without that (output vectors 2i, 2i + 1 of the
+    // call); shorter calls are latency-bound and keep one vector per transform
+    const int64_t per_wave = (int64_t)plan->max_ctas * plan->kernel.groups * plan->kernel.per_unit;
+    cp.pack = plan->data_kind == FIR_OS_REAL && nout >= 2 * per_wave ? 1 : 0;
+    const int64_t per_unit = (int64_t)plan->kernel.per_unit * (cp.pack ? 2 : 1);
+    cp.nunits = (nout + per_unit - 1) / per_unit;
     cp.K = plan->K;
     cp.D = plan->D;
     cp.Nh = plan->Nh;
     cp.P = plan->P;
-    const int64_t want = (cp.nunits + plan->kernel.groups - 1) / plan->kernel.groups;
-    const int64_t grid = want < plan->max_ctas ? want : plan->max_ctas;
+    // one CTA per unit up to one per SM: the kernel deals units across CTAs first
+    const int64_t grid = cp.nunits < plan->max_ctas ? cp.nunits : plan->max_ctas;
     void *args[] = {&cp};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);

@@ -200,9 +200,10 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     int ocur = 0, onxt = 0;           // element offset of the window in the buffer
     bool allow_tma = !p.no_bulk;  // bulk copies read device memory only
 
-    // the groups of all CTAs take work units round-robin
+    // the groups of all CTAs take work units round-robin; a call of fewer units than groups
+    // deals them across CTAs first, so that they spread over every CTA the launch has
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
-    int64_t u = (int64_t)blockIdx.x * C::GROUPS + g;
+    int64_t u = p.nunits < stride ? (int64_t)g * gridDim.x + blockIdx.x : (int64_t)blockIdx.x * C::GROUPS + g;
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
     const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +

@@ -9,6 +9,13 @@
 //
 //   v_k(m) = sum_r h[r K + k] xt[t_m - r K - k],   y[m][q] = sum_k v_k(m) e^{-2 pi i q k / K}.
 //
+// Real input, long calls (p.pack): two consecutive output vectors m, m+1 share one complex
+// transform, their branch sums as the real and imaginary parts (each h[r K + k] read once for
+// both); the two spectra are separated after the transform through Z[K - q]
+// (Y_m[q] = (Z[q] + conj Z[K-q]) / 2, Y_{m+1}[q] = (Z[q] - conj Z[K-q]) / 2i), read back from
+// shared memory.  Short calls, which are latency-bound, keep one vector per transform: twice the
+// transforms in flight, half the serial loads per thread.
+//
 // Thread j of a transform computes v_k for k = j + (K/16) e, e = 0..15 -- exactly the register
 // layout of the K-point Stockham FFT of fos_fft.cuh, which then runs with its twiddles in
 // shared memory (no Tensor Memory: the prototype, not per-thread constants, fills shared
@@ -16,7 +23,7 @@
 // output vectors; a CTA of 512 threads holds 512 / group groups, each with two exchange
 // buffers per transform; the (zero-padded) prototype h[r K + k] lives once per CTA in shared
 // memory.  Grid: persistent, one CTA per SM, units of F output vectors round-robin over all
-// groups.  The input is read through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
+// groups, across CTAs first.  The input is read through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
 #include <type_traits>
 
 #include "fos_chan.h"
@@ -46,7 +53,7 @@ struct ChanCfg {
 // 16 NR loads of x are issued before the first multiply-add.  INTERIOR: every index is inside
 // x, so the loads are one base pointer with constant offsets through the read-only path;
 // otherwise each index is checked and the state (or zero) read in front of x.
-template <int NR, int K, int T, bool REAL, bool INTERIOR, typename T_>
+template <int NR, int K, int T, bool INTERIOR, typename T_>
 __device__ __forceinline__ void branch_taps(float2 (&v)[16], const float *hs, const T_ *x, const T_ *s0,
                                             int64_t hist, int64_t tm, int r0, int j) {
     T_ xv[NR][16];
@@ -74,12 +81,52 @@ __device__ __forceinline__ void branch_taps(float2 (&v)[16], const float *hs, co
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const float hr = hb[q * K + T * e];
-            if constexpr (REAL) {
+            if constexpr (std::is_same<T_, float>::value) {
                 v[e].x = fmaf(hr, xv[q][e], v[e].x);
             } else {
                 v[e].x = fmaf(hr, xv[q][e].x, v[e].x);
                 v[e].y = fmaf(hr, xv[q][e].y, v[e].y);
             }
+        }
+}
+
+// Real input, two output vectors: v[e].x += taps of the vector at t_m = tm, v[e].y += taps of the
+// one at tm + d1 (d1 = D, or 0 when that vector does not exist: it then repeats the first and is
+// not stored), both with the same h[r K + k].  INTERIOR as above, for the first vector.
+template <int NR, int K, int T, bool INTERIOR>
+__device__ __forceinline__ void pair_taps(float2 (&v)[16], const float *hs, const float *x, const float *s0,
+                                          int64_t hist, int64_t tm, int d1, int r0, int j) {
+    float xa[NR][16], xb[NR][16];
+    if constexpr (INTERIOR) {
+        const float *pa = x + (tm - (int64_t)r0 * K - j);
+        const float *pb = pa + d1;
+#pragma unroll
+        for (int q = 0; q < NR; ++q)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                xa[q][e] = __ldg(pa - (q * K + T * e));
+                xb[q][e] = __ldg(pb - (q * K + T * e));
+            }
+    } else {
+#pragma unroll
+        for (int q = 0; q < NR; ++q) {
+            const int64_t tb = tm - (int64_t)(r0 + q) * K - j;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int64_t ta = tb - T * e, tc = ta + d1;
+                xa[q][e] = ta >= 0 ? x[ta] : (ta >= -hist ? s0[hist + ta] : 0.f);
+                xb[q][e] = tc >= 0 ? x[tc] : (tc >= -hist ? s0[hist + tc] : 0.f);
+            }
+        }
+    }
+    const float *hb = hs + r0 * K + j;
+#pragma unroll
+    for (int q = 0; q < NR; ++q)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float hr = hb[q * K + T * e];
+            v[e].x = fmaf(hr, xa[q][e], v[e].x);
+            v[e].y = fmaf(hr, xb[q][e], v[e].y);
         }
 }
 
@@ -110,34 +157,71 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     float2 *y = p.y;
     const int64_t hist = p.Nh - 1;
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
-    for (int64_t u = (int64_t)blockIdx.x * C::GROUPS + g; u < p.nunits; u += stride) {
-        const int64_t m = u * C::F + f;
-        const bool live = m < p.nout;  // a partial last unit: the spare transforms idle
-        const int64_t tm = m * p.D + p.D - 1;
+    // units across CTAs first: a call of fewer units than groups spreads over every CTA
+    for (int64_t u = (int64_t)g * gridDim.x + blockIdx.x; u < p.nunits; u += stride) {
         float2 v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
-        if (live) {
-            // branch sums: v[e] = v_k(m), k = j + T e; several taps of every branch in flight at a
-            // time (four for real input, two for complex), then one tap at a time
-            constexpr int NR = REAL ? 4 : 2;
-            int r = 0;
-            if (tm - (int64_t)p.P * K + 1 >= 0) {  // no branch reaches the state
+        if (REAL && p.pack) {
+            const int64_t m = (u * C::F + f) * 2;  // this transform's vectors m and m + 1
+            const bool live = m < p.nout, live1 = m + 1 < p.nout;
+            const int64_t tm = m * p.D + p.D - 1;
+            if (live) {
+                const float *xr = static_cast<const float *>(p.x), *sr = static_cast<const float *>(p.state);
+                const int d1 = live1 ? p.D : 0;
+                int r = 0;
+                if (tm - (int64_t)p.P * K + 1 >= 0) {
 #pragma unroll 1
-                for (; r + NR <= p.P; r += NR) branch_taps<NR, K, T, REAL, true>(v, hs, x, s0, hist, tm, r, j);
+                    for (; r + 2 <= p.P; r += 2) pair_taps<2, K, T, true>(v, hs, xr, sr, hist, tm, d1, r, j);
 #pragma unroll 1
-                for (; r < p.P; ++r) branch_taps<1, K, T, REAL, true>(v, hs, x, s0, hist, tm, r, j);
-            } else {
+                    for (; r < p.P; ++r) pair_taps<1, K, T, true>(v, hs, xr, sr, hist, tm, d1, r, j);
+                } else {
 #pragma unroll 1
-                for (; r < p.P; ++r) branch_taps<1, K, T, REAL, false>(v, hs, x, s0, hist, tm, r, j);
+                    for (; r < p.P; ++r) pair_taps<1, K, T, false>(v, hs, xr, sr, hist, tm, d1, r, j);
+                }
             }
-        }
-        // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
-        fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
-        if (live) {
-            float2 *ym = y + m * K + j;
+            fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
+            // the transform's last pass reads the other buffer; this one was last read before
+            // that pass's barrier
+            float2 *bz = ((C::S::NPASS - 1) % 2 == 0) ? b0 : b1;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) st_cs(ym + T * e, v[e]);
+            for (int e = 0; e < 16; ++e) bz[xpad(j + T * e)] = v[e];
+            gbar.sync();
+            if (live) {
+                float2 *ym = y + m * K + j;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float2 zc = bz[xpad((K - j - T * e) & (K - 1))];  // Z[K - q]
+                    st_cs(ym + T * e, make_float2(0.5f * (v[e].x + zc.x), 0.5f * (v[e].y - zc.y)));
+                    if (live1) st_cs(ym + K + T * e, make_float2(0.5f * (v[e].y + zc.y), 0.5f * (zc.x - v[e].x)));
+                }
+            }
+        } else {
+            const int64_t m = u * C::F + f;
+            const bool live = m < p.nout;  // a partial last unit: the spare transforms idle
+            const int64_t tm = m * p.D + p.D - 1;
+            if (live) {
+                // branch sums: v[e] = v_k(m), k = j + T e; several taps of every branch in flight
+                // at a time (four for real input, two for complex), then one tap at a time
+                constexpr int NR = REAL ? 4 : 2;
+                int r = 0;
+                if (tm - (int64_t)p.P * K + 1 >= 0) {  // no branch reaches the state
+#pragma unroll 1
+                    for (; r + NR <= p.P; r += NR) branch_taps<NR, K, T, true>(v, hs, x, s0, hist, tm, r, j);
+#pragma unroll 1
+                    for (; r < p.P; ++r) branch_taps<1, K, T, true>(v, hs, x, s0, hist, tm, r, j);
+                } else {
+#pragma unroll 1
+                    for (; r < p.P; ++r) branch_taps<1, K, T, false>(v, hs, x, s0, hist, tm, r, j);
+                }
+            }
+            // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
+            fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
+            if (live) {
+                float2 *ym = y + m * K + j;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) st_cs(ym + T * e, v[e]);
+            }
         }
         gbar.sync();  // the next unit's first pass may write the buffer this one's last pass read
     }

@@ -14,15 +14,16 @@ struct ChanParams {
     const float *h;      // prototype, P K floats (zero beyond Nh)
     const float2 *tw;    // Stockham pass twiddles of the K-point transform
     int64_t nout;        // output vectors: n / D
-    int64_t nunits;      // work units of F output vectors
+    int64_t nunits;      // work units of F transforms
     int K, D, Nh, P;     // channels, decimation, taps, taps per branch (ceil(Nh / K))
+    int pack;            // real input: 1 = two output vectors per transform
 };
 
 struct ChanEntry {
     const void *func = nullptr;
     int threads = 0;
     int groups = 1;      // groups per CTA, each taking units
-    int per_unit = 1;    // output vectors per unit (F)
+    int per_unit = 1;    // transforms per unit (F), each one output vector or (packed) two
     int smem_fixed = 0;  // dynamic shared memory before the prototype
     int tw_entries = 0;  // pass-twiddle table entries
 };

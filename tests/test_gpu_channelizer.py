@@ -5,7 +5,9 @@ max|x| (every output is a sum of Nh products h[l] x, modulated by unit phasors).
 page's two banks (128 and 1024 channels, D = K/2, 2^18 real samples; the 1024-channel one
 sampled), every supported K with real and complex input, decimations other than K/2, prototypes
 that are not a multiple of K, a nonzero initial state, a stream split over calls (equal to one
-call, bit for bit), and the argument checks.
+call, bit for bit), long real-input calls whose transforms carry two output vectors each
+(sampled, including the full-length 2^26-sample stream, and a split that keeps the pairs),
+and the argument checks.
 """
 import numpy as np
 import pytest
@@ -87,7 +89,7 @@ def test_page_bank_1024_sampled():
 ])
 def test_sizes_against_oracle(K, D, Nh, real):
     rng = np.random.Generator(np.random.PCG64(K * 7 + D + Nh))
-    nout = max(3, min(40, (1 << 16) // D, int(3e8) // (K * Nh)))  # bounded oracle work
+    nout = max(3, min(41, (1 << 16) // D, int(3e8) // (K * Nh)))  # bounded oracle work; 41 is odd
     n = nout * D
     h = rng.standard_normal(Nh) / np.sqrt(Nh)
     if real:
@@ -104,17 +106,72 @@ def test_sizes_against_oracle(K, D, Nh, real):
         assert np.array_equal(s, (s_want.real if real else s_want).astype(x.dtype))
 
 
-def test_split_calls_equal_one_call():
+@pytest.mark.parametrize("real", [True, False], ids=["real", "complex"])
+def test_split_calls_equal_one_call(real):
     rng = np.random.Generator(np.random.PCG64(77))
     K, D, Nh = 256, 128, 2048
     n = 64 * D
     h = rng.standard_normal(Nh) / np.sqrt(Nh)
-    x = rng.standard_normal(n).astype(np.float32)
-    s0 = rng.standard_normal(Nh - 1).astype(np.float32)
+    if real:
+        x = rng.standard_normal(n).astype(np.float32)
+        s0 = rng.standard_normal(Nh - 1).astype(np.float32)
+    else:
+        x = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
+        s0 = (rng.standard_normal(Nh - 1) + 1j * rng.standard_normal(Nh - 1)).astype(np.complex64)
     y1, s1 = _run(K, D, h, x, s0)
     y2, s2 = _run(K, D, h, x, s0, calls=[5 * D, 20 * D, 39 * D])
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
     assert np.array_equal(s1, s2)
+
+
+def _pack_threshold(K):
+    """Output vectors from which a real-input call shares each transform between two vectors:
+    twice one wave of transforms (SMs x 512 threads / (K / 16) threads per transform)."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 2 * sms * 512 // (K // 16)
+
+
+def _sampled_vectors(nout, hist_vectors, seed, n_random=24):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    fixed = [0, 1, 2, 3, hist_vectors - 1, hist_vectors, hist_vectors + 1, nout - 3, nout - 2, nout - 1]
+    return np.unique(np.clip(np.concatenate([fixed, rng.integers(0, nout, n_random)]), 0, nout - 1))
+
+
+def test_packed_real_calls():
+    """Real input, calls long enough to pair output vectors in one transform: an odd vector
+    count (the last vector unpaired), a nonzero state, sampled vectors against the oracle
+    (first vectors reading the state, the boundary where the branches leave it, the end), and
+    a split into two calls that keep the pairs, equal to one call bit for bit."""
+    K, D, Nh = 1024, 512, 8192
+    thr = _pack_threshold(K)
+    nout = 2 * thr + 1
+    rng = np.random.Generator(np.random.PCG64(91))
+    h = W.chan_prototype(W.CHANNELIZERS["P2"]).astype(np.float64)
+    x = rng.uniform(-1, 1, nout * D).astype(np.float32)
+    s0 = rng.uniform(-1, 1, Nh - 1).astype(np.float32)
+    y1, st1 = _run(K, D, h, x, s0)
+    ms = _sampled_vectors(nout, Nh // D, seed=5)
+    want = oracle.channelize_at(x, h.astype(np.float32).astype(np.float64), K, D, s0, ms)
+    _check(y1[ms], want, h, x, "packed real, sampled")
+    assert np.array_equal(st1, x[-(Nh - 1):])
+    y2, st2 = _run(K, D, h, x, s0, calls=[thr * D, (nout - thr) * D])
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    assert np.array_equal(st1, st2)
+
+
+def test_page_bank_1024_long_stream_sampled():
+    """The 1024-channel bank over the benchmark's 2^26-sample stream (packed transforms, the
+    benchmark's launch): sampled vectors against the oracle."""
+    c = W.CHANNELIZERS["P2big"]
+    h, x = W.chan_prototype(c), W.chan_x(c)
+    s0 = np.zeros(c.Nh - 1, dtype=x.dtype)
+    assert c.nout >= _pack_threshold(c.K)
+    y, s = _run(c.K, c.D, h, x, s0)
+    ms = _sampled_vectors(c.nout, c.Nh // c.D, seed=6)
+    want = oracle.channelize_at(x, h.astype(np.float32).astype(np.float64), c.K, c.D, s0, ms)
+    _check(y[ms], want, h, x, "P2big sampled")
+    assert np.array_equal(s, x[-(c.Nh - 1):])
 
 
 def test_argument_checks():
