@@ -991,12 +991,16 @@ int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n, void *y, vo
     cp.h = plan->d_h;
     cp.tw = plan->d_tw;
     cp.nout = nout;
-    // real input shares a transform between two output vectors when the call fills every
-    // group of the device at least twice over without that (output vectors 2i, 2i + 1 of the
-    // call); shorter calls are latency-bound and keep one vector per transform
+    // Real input shares a transform between two output vectors (2i, 2i + 1 of the call) when
+    // the call fills every transform slot of the device at least twice over without that, and
+    // with K = 2D a slot takes four vectors (two transforms) when it fills them four times over;
+    // shorter calls are latency-bound and keep one vector per transform.  All three give the
+    // same pairs, so only the unpacked choice changes rounding.
     const int64_t per_wave = (int64_t)plan->max_ctas * plan->kernel.groups * plan->kernel.per_unit;
-    cp.pack = plan->data_kind == FIR_OS_REAL && nout >= 2 * per_wave ? 1 : 0;
-    const int64_t per_unit = (int64_t)plan->kernel.per_unit * (cp.pack ? 2 : 1);
+    cp.pack = 0;
+    if (plan->data_kind == FIR_OS_REAL && nout >= 2 * per_wave)
+        cp.pack = plan->K == 2 * plan->D && nout >= 4 * per_wave ? 2 : 1;
+    const int64_t per_unit = (int64_t)plan->kernel.per_unit * (cp.pack == 2 ? 4 : cp.pack == 1 ? 2 : 1);
     cp.nunits = (nout + per_unit - 1) / per_unit;
     cp.K = plan->K;
     cp.D = plan->D;

@@ -13,8 +13,10 @@
 // transform, their branch sums as the real and imaginary parts (each h[r K + k] read once for
 // both); the two spectra are separated after the transform through Z[K - q]
 // (Y_m[q] = (Z[q] + conj Z[K-q]) / 2, Y_{m+1}[q] = (Z[q] - conj Z[K-q]) / 2i), read back from
-// shared memory.  Short calls, which are latency-bound, keep one vector per transform: twice the
-// transforms in flight, half the serial loads per thread.
+// shared memory.  With K = 2D (the page's 50%-overlapping channels) a thread computes four
+// consecutive vectors, two transforms, whose taps share half their samples (quad_taps).  Short
+// calls, which are latency-bound, keep one vector per transform: more transforms in flight,
+// fewer serial loads per thread.
 //
 // Thread j of a transform computes v_k for k = j + (K/16) e, e = 0..15 -- exactly the register
 // layout of the K-point Stockham FFT of fos_fft.cuh, which then runs with its twiddles in
@@ -130,6 +132,97 @@ __device__ __forceinline__ void pair_taps(float2 (&v)[16], const float *hs, cons
         }
 }
 
+// K = 2D, four vectors m0 .. m0+3 (t = tm + i D): vector m0 + i reads at tap r
+// X(i - 2r) = xt[tm + D (i - 2r) - k], so X(2 - 2r) and X(3 - 2r) are what vectors m0 and m0 + 1
+// read at tap r - 1: each tap loads two new samples and one coefficient per branch for four
+// multiply-adds.  v[e] accumulates vectors m0 (x) and m0 + 1 (y), w[e] vectors m0 + 2 and m0 + 3,
+// each in the same order as pair_taps (taps ascending), so the sums are the pair path's bit for
+// bit.  Every index is inside x (the caller checks).  The branches are taken eight at a time to
+// bound the registers.
+template <int K, int T>
+__device__ __forceinline__ void quad_taps(float2 (&v)[16], float2 (&w)[16], const float *hs, const float *x,
+                                          int64_t tm, int D, int P, int j) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const float *pb = x + (tm - j - (int64_t)T * 8 * hf);  // X(a) of branch e = 8 hf + i: pb[D a - T i]
+        const float *hb = hs + j + T * 8 * hf;
+        float c0[8], c1[8];                                    // X(2 - 2r), X(3 - 2r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c0[i] = __ldg(pb + 2 * D - T * i);
+            c1[i] = __ldg(pb + 3 * D - T * i);
+        }
+#pragma unroll 1
+        for (int r = 0; r < P; ++r) {
+            const float *pr = pb - (int64_t)r * K;
+            float n0[8], n1[8], hr[8];                         // X(-2r), X(1 - 2r), h[r K + k]
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                n0[i] = __ldg(pr - T * i);
+                n1[i] = __ldg(pr + D - T * i);
+                hr[i] = hb[r * K + T * i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = 8 * hf + i;
+                v[e].x = fmaf(hr[i], n0[i], v[e].x);
+                v[e].y = fmaf(hr[i], n1[i], v[e].y);
+                w[e].x = fmaf(hr[i], c0[i], w[e].x);
+                w[e].y = fmaf(hr[i], c1[i], w[e].y);
+                c0[i] = n0[i];
+                c1[i] = n1[i];
+            }
+        }
+    }
+}
+
+// Branch sums of the real-input vectors m (x parts) and m + 1 (y parts) into v, which is zero;
+// nothing for m >= nout, and the second repeats the first when m + 1 >= nout.  NRI taps in
+// flight at a time while no branch reaches the state.
+template <int NRI, int K, int T>
+__device__ __forceinline__ void pair_sums(float2 (&v)[16], const float *hs, const float *x, const float *s0,
+                                          int64_t hist, int64_t m, int64_t nout, int D, int P, int j) {
+    if (m >= nout) return;
+    const int64_t tm = m * D + D - 1;
+    const int d1 = m + 1 < nout ? D : 0;
+    int r = 0;
+    if (tm - (int64_t)P * K + 1 >= 0) {
+#pragma unroll 1
+        for (; r + NRI <= P; r += NRI) pair_taps<NRI, K, T, true>(v, hs, x, s0, hist, tm, d1, r, j);
+#pragma unroll 1
+        for (; r < P; ++r) pair_taps<1, K, T, true>(v, hs, x, s0, hist, tm, d1, r, j);
+    } else {
+#pragma unroll 1
+        for (; r < P; ++r) pair_taps<1, K, T, false>(v, hs, x, s0, hist, tm, d1, r, j);
+    }
+}
+
+// The transform of a packed pair and its split into the spectra of vectors m and m + 1, stored
+// as rows m and m + 1 of y (those below nout).  Starts and ends with the group's buffers free.
+template <int LOGK, class Bar>
+__device__ __forceinline__ void pair_out(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, const Bar &gbar,
+                                         float2 *y, int64_t m, int64_t nout, int j) {
+    constexpr int K = 1 << LOGK, T = K / 16;
+    fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
+    // the transform's last pass reads the other buffer; this one was last read before that
+    // pass's barrier
+    float2 *bz = ((FftShape<LOGK>::NPASS - 1) % 2 == 0) ? b0 : b1;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) bz[xpad(j + T * e)] = v[e];
+    gbar.sync();
+    if (m < nout) {
+        const bool live1 = m + 1 < nout;
+        float2 *ym = y + m * K + j;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float2 zc = bz[xpad((K - j - T * e) & (K - 1))];  // Z[K - q]
+            st_cs(ym + T * e, make_float2(0.5f * (v[e].x + zc.x), 0.5f * (v[e].y - zc.y)));
+            if (live1) st_cs(ym + K + T * e, make_float2(0.5f * (v[e].y + zc.y), 0.5f * (zc.x - v[e].x)));
+        }
+    }
+    gbar.sync();  // the next transform's first pass may write the buffer read here
+}
+
 template <int LOGK, bool REAL>
 __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     using C = ChanCfg<LOGK, REAL>;
@@ -163,38 +256,25 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
         if (REAL && p.pack) {
-            const int64_t m = (u * C::F + f) * 2;  // this transform's vectors m and m + 1
-            const bool live = m < p.nout, live1 = m + 1 < p.nout;
-            const int64_t tm = m * p.D + p.D - 1;
-            if (live) {
-                const float *xr = static_cast<const float *>(p.x), *sr = static_cast<const float *>(p.state);
-                const int d1 = live1 ? p.D : 0;
-                int r = 0;
-                if (tm - (int64_t)p.P * K + 1 >= 0) {
-#pragma unroll 1
-                    for (; r + 2 <= p.P; r += 2) pair_taps<2, K, T, true>(v, hs, xr, sr, hist, tm, d1, r, j);
-#pragma unroll 1
-                    for (; r < p.P; ++r) pair_taps<1, K, T, true>(v, hs, xr, sr, hist, tm, d1, r, j);
+            const float *xr = static_cast<const float *>(p.x), *sr = static_cast<const float *>(p.state);
+            if (p.pack == 2) {  // K = 2D: vectors m .. m + 3, two transforms
+                const int64_t m = (u * C::F + f) * 4;
+                const int64_t tm = m * p.D + p.D - 1;
+                float2 w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = make_float2(0.f, 0.f);
+                if (m + 3 < p.nout && tm - (int64_t)p.P * K + 1 >= 0) {
+                    quad_taps<K, T>(v, w, hs, xr, tm, p.D, p.P, j);
                 } else {
-#pragma unroll 1
-                    for (; r < p.P; ++r) pair_taps<1, K, T, false>(v, hs, xr, sr, hist, tm, d1, r, j);
+                    pair_sums<1, K, T>(v, hs, xr, sr, hist, m, p.nout, p.D, p.P, j);
+                    pair_sums<1, K, T>(w, hs, xr, sr, hist, m + 2, p.nout, p.D, p.P, j);
                 }
-            }
-            fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
-            // the transform's last pass reads the other buffer; this one was last read before
-            // that pass's barrier
-            float2 *bz = ((C::S::NPASS - 1) % 2 == 0) ? b0 : b1;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) bz[xpad(j + T * e)] = v[e];
-            gbar.sync();
-            if (live) {
-                float2 *ym = y + m * K + j;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 zc = bz[xpad((K - j - T * e) & (K - 1))];  // Z[K - q]
-                    st_cs(ym + T * e, make_float2(0.5f * (v[e].x + zc.x), 0.5f * (v[e].y - zc.y)));
-                    if (live1) st_cs(ym + K + T * e, make_float2(0.5f * (v[e].y + zc.y), 0.5f * (zc.x - v[e].x)));
-                }
+                pair_out<LOGK>(v, b0, b1, stw, gbar, y, m, p.nout, j);
+                pair_out<LOGK>(w, b0, b1, stw, gbar, y, m + 2, p.nout, j);
+            } else {  // vectors m, m + 1
+                const int64_t m = (u * C::F + f) * 2;
+                pair_sums<2, K, T>(v, hs, xr, sr, hist, m, p.nout, p.D, p.P, j);
+                pair_out<LOGK>(v, b0, b1, stw, gbar, y, m, p.nout, j);
             }
         } else {
             const int64_t m = u * C::F + f;
@@ -222,8 +302,8 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) st_cs(ym + T * e, v[e]);
             }
+            gbar.sync();  // the next unit's first pass may write the buffer this one's last pass read
         }
-        gbar.sync();  // the next unit's first pass may write the buffer this one's last pass read
     }
 }
 

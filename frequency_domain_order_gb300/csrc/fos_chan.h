@@ -16,7 +16,7 @@ struct ChanParams {
     int64_t nout;        // output vectors: n / D
     int64_t nunits;      // work units of F transforms
     int K, D, Nh, P;     // channels, decimation, taps, taps per branch (ceil(Nh / K))
-    int pack;            // real input: 1 = two output vectors per transform
+    int pack;            // real input: 1 = two output vectors per transform, 2 = four per slot (K = 2D)
 };
 
 struct ChanEntry {

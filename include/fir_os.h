@@ -250,10 +250,11 @@ int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_ki
  * state must not overlap (FIR_OS_E_INVAL).  Launches the channelizer kernel and, when Nh > 1,
  * a one-CTA kernel that writes the new state.  Real input: a call of at least
  * 2 x SMs x 8192 / K output vectors (2432 at K = 1024 on 152 SMs) shares one complex
- * transform between its output vectors 2i and 2i + 1; shorter calls transform each vector
- * alone.  A stream split into calls gives one call's output bit for bit when every call makes
- * the same choice and, for long real-input calls, starts on an even vector; otherwise the
- * results differ in rounding only. */
+ * transform between its output vectors 2i and 2i + 1 (with K = 2D and twice that many vectors,
+ * one thread computes the branch sums of two such transforms, with the same results); shorter
+ * calls transform each vector alone.  A stream split into calls gives one call's output bit
+ * for bit when every call makes the same choice between shared and single transforms and,
+ * for shared ones, starts on an even vector; otherwise the results differ in rounding only. */
 int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n_samples, void *y, void *state,
                      void *stream);
 
