@@ -131,6 +131,32 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, 
     return 0;
 }
 
+// Prefetch into L2 the part of unit u's window that lies in x (rounded inwards to 16 bytes),
+// in 16 pieces issued by threads 0..15 of the group.  A prefetch makes nothing visible to this
+// kernel, so it may run before the wait for the kernel before it: the later gather still reads
+// whatever that kernel wrote.
+template <int LOGN, bool REAL>
+__device__ __forceinline__ void prefetch_unit(const BlockParams &p, const Chan &ch, int64_t u, int tid) {
+    using C = BlockCfg<LOGN, REAL>;
+    constexpr int SB = C::SB, NPF = 16;
+    if (tid >= NPF) return;
+    const int64_t span = (int64_t)C::F * p.L * (REAL ? 2 : 1);
+    int64_t lo = u * span - (p.M - 1);
+    int64_t hi = lo + (int64_t)(REAL ? 2 * C::F - 1 : C::F - 1) * p.L + C::N;
+    if (lo < 0) lo = 0;
+    if (hi > p.n) hi = p.n;
+    if (hi <= lo) return;
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(ch.x);
+    const uintptr_t a0 = (xb + (uintptr_t)lo * SB + 15) & ~uintptr_t(15);
+    const uintptr_t a1 = (xb + (uintptr_t)hi * SB) & ~uintptr_t(15);
+    if (a1 <= a0) return;
+    const uintptr_t piece = ((a1 - a0) / NPF + 15) & ~uintptr_t(15);
+    const uintptr_t b = a0 + (uintptr_t)tid * piece;
+    if (b >= a1) return;
+    const uintptr_t e = b + piece < a1 ? b + piece : a1;
+    prefetch_l2_bulk(reinterpret_cast<const void *>(b), (uint32_t)(e - b));
+}
+
 // S0' = xt[n-(M-1) .. n): samples of x, or (when n < M-1) of S0, which the gather of unit 0
 // left at buffer index (t + M - 1) for xt[t], t < 0.
 template <int LOGN, bool REAL>
@@ -243,10 +269,14 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
         tmem_wait_st();
     }
 
+    int64_t lu = 0, lun = 0;
+    if (u < p.nunits && allow_tma) {
+        const int c0 = channel_of(p, u, lu);
+        prefetch_unit<LOGN, REAL>(p, chan<REAL>(p, c0), lu, tg);
+    }
     // everything above reads plan memory only; x, y and the state may belong to the kernel
     // before this one in the stream, which has to be complete from here on
     griddep_wait();
-    int64_t lu = 0, lun = 0;
     if (u < p.nunits) {
         const int c0 = channel_of(p, u, lu);
         ocur = stage_unit<LOGN, REAL>(p, chan<REAL>(p, c0), lu, cur, bcur, allow_tma, ucur, tg, gbar);
