@@ -101,28 +101,55 @@ __global__ void fos_permute_h(const float2 *H, float2 *Hk, int N, int C) {
     }
 }
 
-// S0' = last M-1 samples of concat(S0, x), in place, one CTA.  Used when the block kernel
-// cannot write the state itself (more than one work unit reads S0).  For n < M-1 the kept
-// part of S0 moves towards the front; chunks are read completely before they are written and
-// every later chunk reads only indices beyond what earlier chunks wrote.
-// One CTA per channel: channel c's x and state start at c * x_stride and c * s_stride.
+// S0' = last `hist` samples of concat(S0, x), in place, for channels blockIdx.y, blockIdx.y +
+// gridDim.y, ... (channel c's x and state start at c * x_stride and c * s_stride).  Used when
+// the kernel that read S0 cannot write the state itself.  n >= hist: a copy of x's tail spread
+// over the CTAs of a row (blockIdx.x).  n < hist: the kept part of S0 moves towards the front,
+// by CTA 0 of the row alone; chunks are read completely before they are written and every
+// later chunk reads only indices beyond what earlier chunks wrote.  Launched with programmatic
+// serialization: it waits for the kernel before it (which reads S0) before touching anything.
 template <typename T>
-__global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist, int64_t x_stride, int64_t s_stride) {
-    x += blockIdx.x * x_stride;
-    state += blockIdx.x * s_stride;
-    if (n >= hist) {
-        for (int t = threadIdx.x; t < hist; t += blockDim.x) state[t] = x[n - hist + t];
-        return;
+__global__ void fos_state_kernel(const T *x, int64_t n, T *state, int hist, int64_t x_stride, int64_t s_stride,
+                                 int channels) {
+    fos::griddep_launch_dependents();
+    fos::griddep_wait();
+    for (int c = blockIdx.y; c < channels; c += gridDim.y) {
+        const T *xc = x + c * x_stride;
+        T *sc = state + c * s_stride;
+        if (n >= hist) {
+            const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+            if (t < hist) sc[t] = xc[n - hist + t];
+            continue;
+        }
+        if (blockIdx.x != 0) continue;
+        const int keep = hist - (int)n;  // samples of S0 that stay
+        for (int c0 = 0; c0 < hist; c0 += blockDim.x) {
+            const int t = c0 + threadIdx.x;
+            T v{};
+            if (t < hist) v = t < keep ? sc[n + t] : xc[t - keep];
+            __syncthreads();
+            if (t < hist) sc[t] = v;
+            __syncthreads();
+        }
     }
-    const int keep = hist - (int)n;  // samples of S0 that stay
-    for (int c0 = 0; c0 < hist; c0 += blockDim.x) {
-        const int t = c0 + threadIdx.x;
-        T v{};
-        if (t < hist) v = t < keep ? state[n + t] : x[t - keep];
-        __syncthreads();
-        if (t < hist) state[t] = v;
-        __syncthreads();
-    }
+}
+
+// Enqueue fos_state_kernel for `channels` channels after the kernel just launched on `stream`.
+template <typename T>
+cudaError_t launch_state(const void *x, int64_t n, void *state, int hist, int64_t xs, int64_t ss, int channels,
+                         cudaStream_t stream) {
+    const bool copy = n >= hist;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(copy ? 256 : 1024);
+    cfg.gridDim = dim3(copy ? (unsigned)((hist + 255) / 256) : 1u, (unsigned)(channels < 65535 ? channels : 65535));
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fos_state_kernel<T>, static_cast<const T *>(x), n, static_cast<T *>(state), hist,
+                              xs, ss, channels);
 }
 
 // ------------------------------------------------------------------ allocation-free response
@@ -322,15 +349,10 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     cfg.numAttrs = na;
     const void *func = channels > 1 && p->kernel.func_multi ? p->kernel.func_multi : p->kernel.func;
     FOS_CUDA(cudaLaunchKernelExC(&cfg, func, args), "block kernel launch");
-    if (!bp.fuse_state && p->M > 1) {
-        if (real)
-            fos_state_kernel<float><<<channels, 1024, 0, stream>>>(static_cast<const float *>(x), n,
-                                                                   static_cast<float *>(state), p->M - 1, xs, ss);
-        else
-            fos_state_kernel<float2><<<channels, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
-                                                                    static_cast<float2 *>(state), p->M - 1, xs, ss);
-        FOS_CUDA(cudaGetLastError(), "state kernel launch");
-    }
+    if (!bp.fuse_state && p->M > 1)
+        FOS_CUDA(real ? launch_state<float>(x, n, state, p->M - 1, xs, ss, channels, stream)
+                      : launch_state<float2>(x, n, state, p->M - 1, xs, ss, channels, stream),
+                 "state kernel launch");
     return FIR_OS_OK;
 }
 
@@ -1022,13 +1044,9 @@ int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n, void *y, vo
     FOS_CUDA(cudaLaunchKernelExC(&cfg, plan->kernel.func, args), "channelizer launch");
     if (hist > 0) {
         // S0' = the last Nh - 1 samples of concat(S0, x), after the filter bank has read S0
-        if (plan->data_kind == FIR_OS_REAL)
-            fos_state_kernel<float><<<1, 1024, 0, stream>>>(static_cast<const float *>(x), n,
-                                                            static_cast<float *>(state), hist, 0, 0);
-        else
-            fos_state_kernel<float2><<<1, 1024, 0, stream>>>(static_cast<const float2 *>(x), n,
-                                                             static_cast<float2 *>(state), hist, 0, 0);
-        FOS_CUDA(cudaGetLastError(), "state kernel launch");
+        FOS_CUDA(plan->data_kind == FIR_OS_REAL ? launch_state<float>(x, n, state, hist, 0, 0, 1, stream)
+                                                : launch_state<float2>(x, n, state, hist, 0, 0, 1, stream),
+                 "state kernel launch");
     }
     return FIR_OS_OK;
 }
