@@ -160,6 +160,31 @@ def test_packed_real_calls():
     assert np.array_equal(st1, st2)
 
 
+@pytest.mark.parametrize("K,D,taps_per_branch", [
+    (64, 32, 8), (256, 128, 8), (4096, 2048, 3),   # K = 2D: four vectors per thread
+    (256, 64, 6), (128, 128, 8), (1024, 300, 5),   # other hops: two vectors per transform
+])
+def test_packed_modes_other_banks(K, D, taps_per_branch):
+    """Long real-input calls of other banks (every thread-group shape from 4 to 256 threads per
+    transform): sampled vectors against the oracle, and a split into two calls of the pair
+    mode equal to the single call bit for bit."""
+    Nh = taps_per_branch * K - K // 3  # not a multiple of K
+    thr = _pack_threshold(K)
+    nout = 2 * thr + 3
+    rng = np.random.Generator(np.random.PCG64(K + D))
+    h = rng.standard_normal(Nh) / np.sqrt(Nh)
+    x = rng.uniform(-1, 1, nout * D).astype(np.float32)
+    s0 = rng.uniform(-1, 1, Nh - 1).astype(np.float32)
+    y1, st1 = _run(K, D, h, x, s0)
+    ms = _sampled_vectors(nout, -(-Nh // D), seed=K + 3 * D)
+    want = oracle.channelize_at(x, h.astype(np.float32).astype(np.float64), K, D, s0, ms)
+    _check(y1[ms], want, h, x, f"K={K} D={D} packed, sampled")
+    assert np.array_equal(st1, x[-(Nh - 1):])
+    y2, st2 = _run(K, D, h, x, s0, calls=[thr * D, (nout - thr) * D])
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    assert np.array_equal(st1, st2)
+
+
 def test_page_bank_1024_long_stream_sampled():
     """The 1024-channel bank over the benchmark's 2^26-sample stream (packed transforms, the
     benchmark's launch): sampled vectors against the oracle."""
