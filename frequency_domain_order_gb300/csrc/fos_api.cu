@@ -964,10 +964,12 @@ int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_ki
     std::vector<float2> tw;
     if (!pass_twiddles(logk, tw)) return bail(fail(FIR_OS_E_UNSUPPORTED, "twiddles"));
     if ((e = cudaMalloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess ||
-        (e = cudaMalloc(&p->d_h, sizeof(float) * Nh)) != cudaSuccess)
+        (e = cudaMalloc(&p->d_h, sizeof(float) * (size_t)P * K)) != cudaSuccess)
         return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc failed"));
+    // the prototype zero-padded to P K taps, so that the kernel reads it in whole 16-byte pieces
     if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice, stream)) !=
             cudaSuccess ||
+        (e = cudaMemsetAsync(p->d_h, 0, sizeof(float) * (size_t)P * K, stream)) != cudaSuccess ||
         (e = cudaMemcpyAsync(p->d_h, h_dev, sizeof(float) * Nh, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
         return bail(cuda_fail(e, "plan upload"));
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "sync"));

@@ -197,32 +197,6 @@ __device__ __forceinline__ void pair_sums(float2 (&v)[16], const float *hs, cons
     }
 }
 
-// The transform of a packed pair and its split into the spectra of vectors m and m + 1, stored
-// as rows m and m + 1 of y (those below nout).  Starts and ends with the group's buffers free.
-template <int LOGK, class Bar>
-__device__ __forceinline__ void pair_out(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, const Bar &gbar,
-                                         float2 *y, int64_t m, int64_t nout, int j) {
-    constexpr int K = 1 << LOGK, T = K / 16;
-    fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
-    // the transform's last pass reads the other buffer; this one was last read before that
-    // pass's barrier
-    float2 *bz = ((FftShape<LOGK>::NPASS - 1) % 2 == 0) ? b0 : b1;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) bz[xpad(j + T * e)] = v[e];
-    gbar.sync();
-    if (m < nout) {
-        const bool live1 = m + 1 < nout;
-        float2 *ym = y + m * K + j;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float2 zc = bz[xpad((K - j - T * e) & (K - 1))];  // Z[K - q]
-            st_cs(ym + T * e, make_float2(0.5f * (v[e].x + zc.x), 0.5f * (v[e].y - zc.y)));
-            if (live1) st_cs(ym + K + T * e, make_float2(0.5f * (v[e].y + zc.y), 0.5f * (zc.x - v[e].x)));
-        }
-    }
-    gbar.sync();  // the next transform's first pass may write the buffer read here
-}
-
 template <int LOGK, bool REAL>
 __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     using C = ChanCfg<LOGK, REAL>;
@@ -239,8 +213,36 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     const typename C::Bar gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
-    for (int i = tid; i < C::TL::SMEM_ENTRIES; i += C::THREADS) stw[i] = p.tw[i];
-    for (int i = tid; i < p.P * K; i += C::THREADS) hs[i] = i < p.Nh ? p.h[i] : 0.f;
+    // plan constants into shared memory: every load of a batch is issued before its stores, so
+    // the latencies overlap (a short call pays this set-up once per CTA)
+    for (int i0 = tid; i0 < C::TL::SMEM_ENTRIES; i0 += 4 * C::THREADS) {
+        float2 t[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * C::THREADS;
+            t[q] = i < C::TL::SMEM_ENTRIES ? p.tw[i] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i0 + q * C::THREADS < C::TL::SMEM_ENTRIES) stw[i0 + q * C::THREADS] = t[q];
+    }
+    {
+        // the prototype, P K floats (zero-padded by the plan), as 16-byte pieces
+        const float4 *h4 = reinterpret_cast<const float4 *>(p.h);
+        float4 *hs4 = reinterpret_cast<float4 *>(hs);
+        const int n4 = p.P * K / 4;
+        for (int i0 = tid; i0 < n4; i0 += 8 * C::THREADS) {
+            float4 t[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * C::THREADS;
+                t[q] = i < n4 ? __ldg(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (i0 + q * C::THREADS < n4) hs4[i0 + q * C::THREADS] = t[q];
+        }
+    }
     __syncthreads();
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
@@ -252,37 +254,45 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
     // units across CTAs first: a call of fewer units than groups spreads over every CTA
     for (int64_t u = (int64_t)g * gridDim.x + blockIdx.x; u < p.nunits; u += stride) {
-        float2 v[16];
+        // branch sums of this slot's transforms (v, and w for the second of a four-vector slot),
+        // then one code path for every transform: a single copy of the FFT in the kernel keeps
+        // its instruction footprint small, which short calls (cold instruction caches) feel
+        float2 v[16], w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
+        for (int e = 0; e < 16; ++e) v[e] = w[e] = make_float2(0.f, 0.f);
+        int64_t m;    // the slot's first output vector
+        int ntr = 1;  // its transforms
         if (REAL && p.pack) {
             const float *xr = static_cast<const float *>(p.x), *sr = static_cast<const float *>(p.state);
             if (p.pack == 2) {  // K = 2D: vectors m .. m + 3, two transforms
-                const int64_t m = (u * C::F + f) * 4;
+                m = (u * C::F + f) * 4;
+                ntr = 2;
                 const int64_t tm = m * p.D + p.D - 1;
-                float2 w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = make_float2(0.f, 0.f);
                 if (m + 3 < p.nout && tm - (int64_t)p.P * K + 1 >= 0) {
                     quad_taps<K, T>(v, w, hs, xr, tm, p.D, p.P, j);
                 } else {
-                    pair_sums<1, K, T>(v, hs, xr, sr, hist, m, p.nout, p.D, p.P, j);
-                    pair_sums<1, K, T>(w, hs, xr, sr, hist, m + 2, p.nout, p.D, p.P, j);
+                    // the second pair first, kept in w, then the first pair
+#pragma unroll 1
+                    for (int t = 1; t >= 0; --t) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = make_float2(0.f, 0.f);
+                        pair_sums<1, K, T>(v, hs, xr, sr, hist, m + 2 * t, p.nout, p.D, p.P, j);
+                        if (t == 1) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) w[e] = v[e];
+                        }
+                    }
                 }
-                pair_out<LOGK>(v, b0, b1, stw, gbar, y, m, p.nout, j);
-                pair_out<LOGK>(w, b0, b1, stw, gbar, y, m + 2, p.nout, j);
             } else {  // vectors m, m + 1
-                const int64_t m = (u * C::F + f) * 2;
+                m = (u * C::F + f) * 2;
                 pair_sums<2, K, T>(v, hs, xr, sr, hist, m, p.nout, p.D, p.P, j);
-                pair_out<LOGK>(v, b0, b1, stw, gbar, y, m, p.nout, j);
             }
         } else {
-            const int64_t m = u * C::F + f;
-            const bool live = m < p.nout;  // a partial last unit: the spare transforms idle
+            m = u * C::F + f;
             const int64_t tm = m * p.D + p.D - 1;
-            if (live) {
-                // branch sums: v[e] = v_k(m), k = j + T e; several taps of every branch in flight
-                // at a time (four for real input, two for complex), then one tap at a time
+            if (m < p.nout) {  // a partial last unit: the spare transforms idle
+                // v[e] = v_k(m), k = j + T e; several taps of every branch in flight at a time
+                // (four for real input, two for complex), then one tap at a time
                 constexpr int NR = REAL ? 4 : 2;
                 int r = 0;
                 if (tm - (int64_t)p.P * K + 1 >= 0) {  // no branch reaches the state
@@ -295,14 +305,40 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
                     for (; r < p.P; ++r) branch_taps<1, K, T, false>(v, hs, x, s0, hist, tm, r, j);
                 }
             }
-            // the K-point DFT across the branches (forward, unscaled): Y[j + T e] in v[e]
+        }
+#pragma unroll 1
+        for (int t = 0; t < ntr; ++t) {
+            if (t == 1) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = w[e];
+            }
+            const int64_t mt = m + 2 * t;
+            // the K-point DFT across the branches (forward, unscaled): Z[j + T e] in v[e]
             fft_tm<LOGK, (1 << 30), false>(v, b0, b1, stw, 0u, j, gbar);
-            if (live) {
-                float2 *ym = y + m * K + j;
+            if (REAL && p.pack) {
+                // Z[K - q] through shared memory: the transform's last pass reads the other
+                // buffer; this one was last read before that pass's barrier
+                float2 *bz = ((C::S::NPASS - 1) % 2 == 0) ? b0 : b1;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) bz[xpad(j + T * e)] = v[e];
+                gbar.sync();
+                if (mt < p.nout) {
+                    const bool live1 = mt + 1 < p.nout;
+                    float2 *ym = y + mt * K + j;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 zc = bz[xpad((K - j - T * e) & (K - 1))];
+                        st_cs(ym + T * e, make_float2(0.5f * (v[e].x + zc.x), 0.5f * (v[e].y - zc.y)));
+                        if (live1)
+                            st_cs(ym + K + T * e, make_float2(0.5f * (v[e].y + zc.y), 0.5f * (zc.x - v[e].x)));
+                    }
+                }
+            } else if (mt < p.nout) {
+                float2 *ym = y + mt * K + j;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) st_cs(ym + T * e, v[e]);
             }
-            gbar.sync();  // the next unit's first pass may write the buffer this one's last pass read
+            gbar.sync();  // the next transform's first pass may write the buffers read here
         }
     }
 }
