@@ -152,6 +152,24 @@ cudaError_t launch_state(const void *x, int64_t n, void *state, int hist, int64_
                               xs, ss, channels);
 }
 
+// Measurement aid for the FP32 roofline: eight independent multiply-add chains per thread, so
+// that every SM's FP32 lanes stay busy.  The sum is stored only if it equals -1, which the
+// chains never reach (every value stays positive); the compiler cannot drop them.
+__global__ void __launch_bounds__(1024) fos_fp32_probe_kernel(float *sink, int iters) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 1.0f + 1e-3f * (float)(threadIdx.x + i);
+    const float b = 0.9999f, c = 1e-4f;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = fmaf(a[i], b, c);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += a[i];
+    if (s == -1.0f) sink[blockIdx.x] = s;
+}
+
 // ------------------------------------------------------------------ allocation-free response
 // fir_os_frequency_response_noalloc runs the float64 step-1 transform above with its two
 // ping-pong buffers taken from this fixed device array instead of cudaMalloc.  Every device
@@ -854,6 +872,21 @@ int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n, void 
     FOS_CUDA(cudaStreamSynchronize(plan->s_in), "sync");
     FOS_CUDA(cudaStreamSynchronize(plan->s_comp), "sync");
     FOS_CUDA(cudaStreamSynchronize(plan->s_out), "sync");
+    return FIR_OS_OK;
+}
+
+int fir_os_fp32_probe(int iters, void *stream_, double *flops) {
+    if (iters < 1 || !flops) return fail(FIR_OS_E_INVAL, "iters must be >= 1 and flops non-NULL");
+    int dev = 0, sms = 0, per_sm = 0;
+    FOS_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    FOS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
+    FOS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fos_fp32_probe_kernel, 1024, 0),
+             "occupancy query");
+    if (per_sm < 1) per_sm = 1;
+    const int grid = sms * per_sm;
+    fos_fp32_probe_kernel<<<grid, 1024, 0, static_cast<cudaStream_t>(stream_)>>>(nullptr, iters);
+    FOS_CUDA(cudaGetLastError(), "probe launch");
+    *flops = 2.0 * 8.0 * 1024.0 * (double)grid * (double)iters;
     return FIR_OS_OK;
 }
 

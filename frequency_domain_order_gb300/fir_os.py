@@ -45,6 +45,7 @@ SIGNATURES = {
     "fir_os_frequency_response_noalloc": (_I, [_P, _I, _I, _I, _P, _P]),
     "fir_os_choose_n": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
     "fir_os_predict_gsps": (_I, [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_double)]),
+    "fir_os_fp32_probe": (_I, [_I, _P, ctypes.POINTER(ctypes.c_double)]),
     "fir_chan_plan_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _P, _P]),
     "fir_chan_execute": (_I, [_P, _P, _I64, _P, _P, _P]),
     "fir_chan_plan_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
@@ -69,6 +70,13 @@ def predict_gsps(M: int, N: int, real: bool = False, sms: int = 0) -> float:
     g = ctypes.c_double()
     _check(lib().fir_os_predict_gsps(int(M), int(N), REAL if real else COMPLEX, int(sms), ctypes.byref(g)))
     return g.value
+
+
+def fp32_probe(iters: int, stream=None) -> float:
+    """fir_os_fp32_probe: enqueue the FP32 multiply-add probe on `stream`; returns its flops."""
+    f = ctypes.c_double()
+    _check(lib().fir_os_fp32_probe(int(iters), _stream_handle(stream), ctypes.byref(f)))
+    return f.value
 
 
 class FirOsError(RuntimeError):

@@ -149,6 +149,14 @@ int fir_os_execute_batched(fir_os_plan_t plan, const void *x, int64_t x_stride, 
 int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n_samples,
                         void *y_host, void *state_host, void *stream);
 
+/* fir_os_fp32_probe -- a measurement aid, not a step of the method: enqueues on `stream` one
+ * kernel of independent float32 multiply-add chains (eight per thread, 1024 threads per CTA, as
+ * many CTAs as are resident on every SM at once) running `iters` iterations, for measuring the
+ * FP32 peak that the filter's arithmetic roofline is taken against.  The caller times it (for
+ * example with events on `stream`).  *flops receives the floating-point operations the kernel
+ * performs (two per multiply-add).  FIR_OS_E_INVAL for iters < 1 or flops NULL. */
+int fir_os_fp32_probe(int iters, void *stream, double *flops);
+
 /* fir_os_plan_destroy -- synchronises the device work of the plan and frees it. NULL is a
  * no-op. */
 int fir_os_plan_destroy(fir_os_plan_t plan);

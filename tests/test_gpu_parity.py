@@ -334,3 +334,29 @@ def test_runtime_argument_checks():
         fir_os.Plan(M, N, Hc, real=True, coef_kind=fir_os.COEF_FREQ)
     assert e.value.status == fir_os.E_UNSUPPORTED
     plan.device_status()
+
+
+# ----------------------------------------------------------------------------- measurement aid
+
+
+def test_fp32_probe_measures_a_plausible_peak():
+    """fir_os_fp32_probe: the flops it reports over its event-timed duration give a peak between
+    a tenth of and twice the nominal SMs x 128 lanes x 2 x max clock; bad arguments are rejected."""
+    torch = pytest.importorskip("torch")
+    from frequency_domain_order_gb300 import fir_os
+    import ctypes
+    stream = torch.cuda.current_stream()
+    fir_os.fp32_probe(256, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    flops = fir_os.fp32_probe(8192, stream)
+    b.record(stream)
+    b.synchronize()
+    tflops = flops / (a.elapsed_time(b) * 1e-3) / 1e12
+    props = torch.cuda.get_device_properties(0)
+    nominal = props.multi_processor_count * 128 * 2 * 2.2e9 / 1e12
+    assert flops > 0 and 0.1 * nominal < tflops < 2 * nominal, (tflops, nominal)
+    L = fir_os.lib()
+    f = ctypes.c_double()
+    assert L.fir_os_fp32_probe(0, None, ctypes.byref(f)) == fir_os.E_INVAL
+    assert L.fir_os_fp32_probe(16, None, None) == fir_os.E_INVAL
