@@ -87,8 +87,8 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, 
     const int64_t span = (int64_t)C::F * p.L * (REAL ? 2 : 1);
     const int64_t start = u * span - (p.M - 1);
     const int64_t len = (int64_t)(REAL ? 2 * C::F - 1 : C::F - 1) * p.L + C::N;
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(ch.x);
     if (allow_tma && start >= 0) {
-        const uintptr_t xb = reinterpret_cast<uintptr_t>(ch.x);
         const uintptr_t a0 = xb + (uintptr_t)start * SB, a1 = a0 + (uintptr_t)len * SB;
         const uintptr_t b0 = a0 & ~uintptr_t(15), b1 = (a1 + 15) & ~uintptr_t(15);
         if (b0 >= xb && b1 <= xb + (uintptr_t)p.n * SB) {
@@ -101,11 +101,46 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, 
             return (int)((a0 - b0) / SB);
         }
     }
-    used_tma = false;
-    const int64_t hist = p.M - 1;
     using T_ = typename std::conditional<REAL, float, float2>::type;
     const T_ *x = static_cast<const T_ *>(ch.x);
     const T_ *s0 = static_cast<const T_ *>(ch.state);
+    const int64_t hist = p.M - 1;
+    if (allow_tma) {
+        // a window that reaches the state or the end of x: the part inside x, rounded inwards to
+        // 16 bytes, by one bulk copy, placed so that its buffer address is 16-byte aligned;
+        // the rest (state samples, at most three samples at either end of that part, zeros
+        // past x) by plain loads of the group
+        const int64_t xs = start > 0 ? start : 0, xe = start + len < p.n ? start + len : p.n;
+        const uintptr_t c0 = (xb + (uintptr_t)xs * SB + 15) & ~uintptr_t(15);
+        const uintptr_t c1 = (xb + (uintptr_t)xe * SB) & ~uintptr_t(15);
+        if (xe > xs && c1 > c0) {
+            const int64_t i0 = (int64_t)((c0 - xb) / SB) - start;  // window index of the copy's first sample
+            const int64_t i1 = (int64_t)((c1 - xb) / SB) - start;
+            const int off = (int)((16 - (i0 * SB) % 16) % 16) / SB;  // buffer index of window index 0
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, (uint32_t)(c1 - c0));
+                bulk_g2s(buf + (off + i0) * SB, reinterpret_cast<const void *>(c0), (uint32_t)(c1 - c0), bar);
+            }
+            T_ *dst = reinterpret_cast<T_ *>(buf) + off;
+            for (int h = 0; h < 2; ++h) {  // window indices [0, i0), then [i1, len)
+                for (int64_t i = (h ? i1 : 0) + tid; i < (h ? len : i0); i += C::GT) {
+                    const int64_t t = start + i;
+                    T_ v{};
+                    if (t >= 0) {
+                        if (t < p.n) v = x[t];
+                    } else if (t >= -hist) {
+                        v = s0[hist + t];
+                    }
+                    dst[i] = v;
+                }
+            }
+            gbar.sync();
+            used_tma = true;
+            return off;
+        }
+    }
+    used_tma = false;
     T_ *dst = reinterpret_cast<T_ *>(buf);
     // batches of independent loads, so their latencies overlap instead of adding up
     constexpr int U = 8;
@@ -132,14 +167,14 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, 
 }
 
 // Prefetch into L2 the part of unit u's window that lies in x (rounded inwards to 16 bytes),
-// in 16 pieces issued by threads 0..15 of the group.  A prefetch makes nothing visible to this
+// one instruction issued by thread 0 of the group (issuing costs time; the window is small).  A prefetch makes nothing visible to this
 // kernel, so it may run before the wait for the kernel before it: the later gather still reads
 // whatever that kernel wrote.
 template <int LOGN, bool REAL>
 __device__ __forceinline__ void prefetch_unit(const BlockParams &p, const Chan &ch, int64_t u, int tid) {
     using C = BlockCfg<LOGN, REAL>;
-    constexpr int SB = C::SB, NPF = 16;
-    if (tid >= NPF) return;
+    constexpr int SB = C::SB;
+    if (tid != 0) return;
     const int64_t span = (int64_t)C::F * p.L * (REAL ? 2 : 1);
     int64_t lo = u * span - (p.M - 1);
     int64_t hi = lo + (int64_t)(REAL ? 2 * C::F - 1 : C::F - 1) * p.L + C::N;
@@ -150,22 +185,18 @@ __device__ __forceinline__ void prefetch_unit(const BlockParams &p, const Chan &
     const uintptr_t a0 = (xb + (uintptr_t)lo * SB + 15) & ~uintptr_t(15);
     const uintptr_t a1 = (xb + (uintptr_t)hi * SB) & ~uintptr_t(15);
     if (a1 <= a0) return;
-    const uintptr_t piece = ((a1 - a0) / NPF + 15) & ~uintptr_t(15);
-    const uintptr_t b = a0 + (uintptr_t)tid * piece;
-    if (b >= a1) return;
-    const uintptr_t e = b + piece < a1 ? b + piece : a1;
-    prefetch_l2_bulk(reinterpret_cast<const void *>(b), (uint32_t)(e - b));
+    prefetch_l2_bulk(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
 }
 
 // S0' = xt[n-(M-1) .. n): samples of x, or (when n < M-1) of S0, which the gather of unit 0
-// left at buffer index (t + M - 1) for xt[t], t < 0.
+// left at buffer index off + (t + M - 1) for xt[t], t < 0.
 template <int LOGN, bool REAL>
 __device__ __forceinline__ void write_state(const BlockParams &p, const Chan &ch, const unsigned char *buf,
-                                            int tid) {
+                                            int off, int tid) {
     using C = BlockCfg<LOGN, REAL>;
     using T_ = typename std::conditional<REAL, float, float2>::type;
     const T_ *x = static_cast<const T_ *>(ch.x);
-    const T_ *stg = reinterpret_cast<const T_ *>(buf);
+    const T_ *stg = reinterpret_cast<const T_ *>(buf) + off;
     T_ *st = static_cast<T_ *>(ch.state);
     const int hist = p.M - 1;
     constexpr int U = 8;  // independent loads in flight per thread
@@ -316,7 +347,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = sc[e * T];
         }
-        if (p.fuse_state && lu == 0) write_state<LOGN, REAL>(p, chan<REAL>(p, chu), cur, tg);
+        if (p.fuse_state && lu == 0) write_state<LOGN, REAL>(p, chan<REAL>(p, chu), cur, ocur, tg);
 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
