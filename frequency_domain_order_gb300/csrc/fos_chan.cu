@@ -301,6 +301,26 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
 #pragma unroll 1
                     for (; r < p.P; ++r) branch_taps<1, K, T, true>(v, hs, x, s0, hist, tm, r, j);
                 } else {
+                    // the window reaches the state.  Tap r reads xt[tm - rK - (K-1) .. tm - rK]:
+                    // taps below rx lie inside x, tap rx may straddle x[0], the taps below rs lie
+                    // inside the state (read with the same batched loads, from the state's end),
+                    // and only the straddling tap and taps reaching below the state (prototype
+                    // padding) take checked loads
+                    const int rx = (int)((tm + 1) / K);
+                    const int rs = (int)((tm + hist + 1) / K) < p.P ? (int)((tm + hist + 1) / K) : p.P;
+                    const T_ *se = s0 + hist;  // xt[t] = se[t] for -hist <= t < 0
+#pragma unroll 1
+                    for (; r + NR <= rx; r += NR) branch_taps<NR, K, T, true>(v, hs, x, s0, hist, tm, r, j);
+#pragma unroll 1
+                    for (; r < rx; ++r) branch_taps<1, K, T, true>(v, hs, x, s0, hist, tm, r, j);
+                    if (r < p.P && tm - (int64_t)r * K >= 0) {
+                        branch_taps<1, K, T, false>(v, hs, x, s0, hist, tm, r, j);
+                        ++r;
+                    }
+#pragma unroll 1
+                    for (; r + NR <= rs; r += NR) branch_taps<NR, K, T, true>(v, hs, se, s0, hist, tm, r, j);
+#pragma unroll 1
+                    for (; r < rs; ++r) branch_taps<1, K, T, true>(v, hs, se, s0, hist, tm, r, j);
 #pragma unroll 1
                     for (; r < p.P; ++r) branch_taps<1, K, T, false>(v, hs, x, s0, hist, tm, r, j);
                 }
