@@ -24,8 +24,9 @@
 // memory).  A group of max(64, K/16) threads transforms F = max(1, 64 / (K/16)) consecutive
 // output vectors; a CTA of 512 threads holds 512 / group groups, each with two exchange
 // buffers per transform; the (zero-padded) prototype h[r K + k] lives once per CTA in shared
-// memory.  Grid: persistent, one CTA per SM, units of F output vectors round-robin over all
-// groups, across CTAs first.  The input is read through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
+// memory.  Grid: persistent, one CTA per SM; work units of F transform slots (each one, two or
+// four output vectors) round-robin over all groups, across CTAs first.  The input is read
+// through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
 #include <type_traits>
 
 #include "fos_chan.h"
@@ -52,9 +53,10 @@ struct ChanCfg {
 };
 
 // v[e] += sum over taps r0 .. r0 + NR - 1 of h[r K + k] xt[t_m - r K - k], k = j + T e: all
-// 16 NR loads of x are issued before the first multiply-add.  INTERIOR: every index is inside
-// x, so the loads are one base pointer with constant offsets through the read-only path;
-// otherwise each index is checked and the state (or zero) read in front of x.
+// 16 NR loads are issued before the first multiply-add.  INTERIOR: every index lies in the
+// array that x points into (x itself, or the state when x is passed as the state's end), so the
+// loads are one base pointer with constant offsets through the read-only path; otherwise each
+// index is checked and the state (or zero) read in front of x.
 template <int NR, int K, int T, bool INTERIOR, typename T_>
 __device__ __forceinline__ void branch_taps(float2 (&v)[16], const float *hs, const T_ *x, const T_ *s0,
                                             int64_t hist, int64_t tm, int r0, int j) {
