@@ -262,6 +262,21 @@ def fp32_block(achieved_tflops: float, peak_tflops: float, nominal_tflops: float
                 frac=achieved_tflops / peak_tflops)
 
 
+def steps_per_graph(sets: int, launches_per_step: int, max_launches: int = 2048) -> int:
+    """Consecutive steps captured in one CUDA graph: a multiple of the buffer sets (a replay ends
+    on the set it began with), at least 8 steps, at most ~max_launches kernel launches."""
+    r = sets * max(1, -(-8 // sets))
+    while r > sets and r * launches_per_step > max_launches:
+        r -= sets
+    return r
+
+
+def graph_replays(K: int, R: int):
+    """(steps of each replay) covering exactly K steps: full replays of R, then the remainder."""
+    full, rem = divmod(K, R)
+    return [R] * full + ([rem] if rem else [])
+
+
 def step_stats(durations_ms):
     """(median, 20th percentile) of per-step device times in ms."""
     d = sorted(durations_ms)
@@ -337,59 +352,62 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
             off += c
 
     ncall = len(w.calls)
+    K = args.steps
     graphs = None
     if not args.direct:
-        # capture each buffer set's calls once into a CUDA graph and replay it: a step of small
-        # calls is otherwise bound by the Python launch path, and an event pair around a direct
-        # launch includes the host's launch latency (the calls are plain kernel launches)
+        # consecutive steps (cycling through the buffer sets) captured into CUDA graphs and
+        # replayed: one graph launch per R steps instead of per step, and programmatic dependent
+        # launch overlaps each call's set-up with the previous call's end across step boundaries
+        # too.  Every step still runs every call of the workload.
         for k in range(sets):
             step(k)
         torch.cuda.synchronize()
-        graphs = []
-        for k in range(sets):
+        R = steps_per_graph(sets, ncall)
+
+        def capture(nsteps):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 cap = torch.cuda.current_stream(dev)
-                off = 0
-                for c in w.calls:
-                    call(k, off, c, cap)
-                    off += c
-            graphs.append(g)
-
-    def run_step(i, evs=None):
-        if graphs is None:
-            step(i, evs)
-        else:
-            if evs is not None:
-                evs[0][0].record(stream)
-            graphs[i % sets].replay()
-            if evs is not None:
-                evs[0][1].record(stream)
-
-    for i in range(args.warmup):
-        run_step(i)
+                for i in range(nsteps):
+                    off = 0
+                    for c in w.calls:
+                        call(i % sets, off, c, cap)
+                        off += c
+            return g
+        graphs = {n: capture(n) for n in set(graph_replays(K, R))}
+        for _ in range(-(-args.warmup // max(graphs))):
+            graphs[max(graphs)].replay()
+    else:
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
     plan.device_status()
 
-    K = args.steps
+    runs = graph_replays(K, R) if graphs is not None else [1] * K
     nev = 1 if graphs is not None else ncall
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(nev)] for _ in range(K)]
+           for _ in range(nev)] for _ in runs]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
-        hold_stream(K)
-        for i in range(K):
-            run_step(i, ev[i])
+        hold_stream(len(runs))
+        for i, n in enumerate(runs):
+            if graphs is None:
+                step(i, ev[i])
+            else:
+                ev[i][0][0].record(stream)
+                graphs[n].replay()
+                ev[i][0][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier(world)
     plan.device_status()
     total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1])
-    # each call is one launch of the block kernel (the state is written in-kernel); with a
-    # graph the per-launch time is the step's device time over its launches
-    launch_ms = statistics.fmean(a.elapsed_time(b) for step_ev in ev for a, b in step_ev) / (ncall // nev)
+    # per launch of the block kernel (each call is one launch; the state is written in-kernel):
+    # the timed device time over the launches it holds
+    launch_ms = total_ms / (K * ncall)
+    step_ms = [s_ev[0][0].elapsed_time(s_ev[-1][1]) / n for s_ev, n in zip(ev, runs)]
     ms_step = reduce_max(total_ms / K, world, dev)
     launches_per_step = sum(plan.launches(c) for c in w.calls)
 
@@ -405,7 +423,7 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_nominal = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
     fp32_peak = measure_fp32_peak(stream)
-    med_ms, p20_ms = step_stats([s_ev[0][0].elapsed_time(s_ev[-1][1]) for s_ev in ev])
+    med_ms, p20_ms = step_stats(step_ms)
     flops_step = total * flops_per_output(w)
     t_hbm = bytes_step / (peak * 1e9)
     t_fp32 = flops_step / (fp32_peak * 1e12)
@@ -468,7 +486,9 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
                             "frac": max(t_hbm, t_fp32) / (ms_step * 1e-3)},
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
-        "launch_mode": "CUDA graph of the step's calls, replayed" if graphs is not None else "direct launches",
+        "launch_mode": (f"CUDA graphs of {max(runs)} consecutive steps (cycling through the buffer sets), "
+                        f"replayed {len(runs)} times; per-step median and p20 are over replays"
+                        if graphs is not None else "direct launches"),
         "clocks": clk,
         "kernel": plan.kernel(),
         "wall_s_timed_region": wall,
@@ -619,31 +639,38 @@ def run_chan(args, c, world: int, rank: int, local: int):
     for k in range(sets):
         plan.execute(xs[k], ys[k], sts[k], stream)
     torch.cuda.synchronize()
-    graphs = []
-    for k in range(sets):
+    # consecutive steps (cycling through the buffer sets) captured into CUDA graphs, as for the
+    # filter: one graph launch per R steps
+    K = args.steps
+    R = steps_per_graph(sets, 2)
+
+    def capture(nsteps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            plan.execute(xs[k], ys[k], sts[k], torch.cuda.current_stream(dev))
-        graphs.append(g)
-    for i in range(args.warmup):
-        graphs[i % sets].replay()
+            for i in range(nsteps):
+                plan.execute(xs[i % sets], ys[i % sets], sts[i % sets], torch.cuda.current_stream(dev))
+        return g
+    runs = graph_replays(K, R)
+    graphs = {n: capture(n) for n in set(runs)}
+    for _ in range(-(-args.warmup // max(graphs))):
+        graphs[max(graphs)].replay()
     torch.cuda.synchronize()
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in runs]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
-        hold_stream(K)
-        for i in range(K):
-            ev[i][0].record(stream)
-            graphs[i % sets].replay()
-            ev[i][1].record(stream)
+        hold_stream(len(runs))
+        for (a, b), n in zip(ev, runs):
+            a.record(stream)
+            graphs[n].replay()
+            b.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier(world)
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    launch_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    launch_ms = total_ms / K  # per call (the filter-bank kernel and the state kernel)
+    step_ms = [a.elapsed_time(b) / n for (a, b), n in zip(ev, runs)]
     ms_step = reduce_max(total_ms / K, world, dev)
     value = world * c.n / (ms_step * 1e-3) / 1e9
     peak, peak_kind, peaks = measured_peaks()
@@ -654,7 +681,7 @@ def run_chan(args, c, world: int, rank: int, local: int):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_nominal = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
     fp32_peak = measure_fp32_peak(stream)
-    med_ms, p20_ms = step_stats([a.elapsed_time(b) for a, b in ev])
+    med_ms, p20_ms = step_stats(step_ms)
     flops_step = c.n * chan_flops_per_input(c)
     t_hbm = bytes_step / (peak * 1e9)
     t_fp32 = flops_step / (fp32_peak * 1e12)
@@ -703,7 +730,8 @@ def run_chan(args, c, world: int, rank: int, local: int):
                 "h2d_bytes_per_step": x.nbytes, "d2h_bytes_per_step": c.nout * c.K * 8, "steps": e2e_steps,
                 "path": "pinned input copied in, fir_chan_execute, output copied back"},
         "gpu_launches": K * (2 if c.Nh > 1 else 1),
-        "launch_mode": "CUDA graph of the call, replayed",
+        "launch_mode": (f"CUDA graphs of {max(runs)} consecutive calls (cycling through the buffer sets), "
+                        f"replayed {len(runs)} times; per-step median and p20 are over replays"),
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
