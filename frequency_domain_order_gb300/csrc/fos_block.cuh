@@ -260,7 +260,16 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     // the groups of all CTAs take work units round-robin; a call of fewer units than groups
     // deals them across CTAs first, so that they spread over every CTA the launch has
     const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
-    int64_t u = p.nunits < stride ? (int64_t)g * gridDim.x + blockIdx.x : (int64_t)blockIdx.x * C::GROUPS + g;
+    int64_t u, ustep, uend;
+    if (p.nunits < stride) {  // at most one unit per group, dealt across CTAs first
+        u = (int64_t)g * gridDim.x + blockIdx.x;
+        ustep = stride;
+        uend = p.nunits;
+    } else {  // a contiguous range of units per CTA, its groups taking them in turn
+        u = blockIdx.x * p.nunits / gridDim.x + g;
+        ustep = C::GROUPS;
+        uend = (blockIdx.x + 1) * p.nunits / gridDim.x;
+    }
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
     const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
@@ -301,14 +310,14 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     }
 
     int64_t lu = 0, lun = 0;
-    if (u < p.nunits && allow_tma) {
+    if (u < uend && allow_tma) {
         const int c0 = channel_of(p, u, lu);
         prefetch_unit<LOGN, REAL>(p, chan<REAL>(p, c0), lu, tg);
     }
     // everything above reads plan memory only; x, y and the state may belong to the kernel
     // before this one in the stream, which has to be complete from here on
     griddep_wait();
-    if (u < p.nunits) {
+    if (u < uend) {
         const int c0 = channel_of(p, u, lu);
         ocur = stage_unit<LOGN, REAL>(p, chan<REAL>(p, c0), lu, cur, bcur, allow_tma, ucur, tg, gbar);
     }
@@ -316,10 +325,10 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     // outputs t = j + e T with t >= M - 1 are kept: e >= e_keep
     const int e_keep = (p.M - 1 - j + T - 1) < 0 ? 0 : (p.M - 1 - j + T - 1) / T;
 
-    for (; u < p.nunits; u += stride) {
+    for (; u < uend; u += ustep) {
         const int chu = channel_of(p, u, lu);  // this unit's channel
-        const int64_t un = u + stride;
-        if (un < p.nunits) {
+        const int64_t un = u + ustep;
+        if (un < uend) {
             const int chn = channel_of(p, un, lun);
             onxt = stage_unit<LOGN, REAL>(p, chan<REAL>(p, chn), lun, nxt, bnxt, allow_tma, unxt, tg, gbar);
         }
