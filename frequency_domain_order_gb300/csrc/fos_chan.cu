@@ -25,8 +25,8 @@
 // output vectors; a CTA of 512 threads holds 512 / group groups, each with two exchange
 // buffers per transform; the (zero-padded) prototype h[r K + k] lives once per CTA in shared
 // memory.  Grid: persistent, one CTA per SM; work units of F transform slots (each one, two or
-// four output vectors) round-robin over all groups, across CTAs first.  The input is read
-// through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
+// four output vectors) in a contiguous range per CTA, its groups taking them in turn.  The
+// input is read through L1/L2 (each sample feeds ceil(Nh / D) output vectors).
 #include <type_traits>
 
 #include "fos_chan.h"
@@ -253,9 +253,10 @@ __global__ void __launch_bounds__(512, 1) fos_chan_kernel(const ChanParams p) {
     const T_ *s0 = static_cast<const T_ *>(p.state);
     float2 *y = p.y;
     const int64_t hist = p.Nh - 1;
-    const int64_t stride = (int64_t)gridDim.x * C::GROUPS;
-    // units across CTAs first: a call of fewer units than groups spreads over every CTA
-    for (int64_t u = (int64_t)g * gridDim.x + blockIdx.x; u < p.nunits; u += stride) {
+    // each CTA takes a contiguous range of units (the launch has at most one CTA per unit), its
+    // groups taking them in turn, so that the groups of an SM read overlapping windows
+    const int64_t uend = (blockIdx.x + 1) * p.nunits / gridDim.x;
+    for (int64_t u = blockIdx.x * p.nunits / gridDim.x + g; u < uend; u += C::GROUPS) {
         // branch sums of this slot's transforms (v, and w for the second of a four-vector slot),
         // then one code path for every transform: a single copy of the FFT in the kernel keeps
         // its instruction footprint small, which short calls (cold instruction caches) feel

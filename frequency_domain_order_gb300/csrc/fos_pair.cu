@@ -211,10 +211,13 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     const GroupBarrier<256> gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
-    int64_t u = cluster_id_x(), lu = 0, lun = 0;
+    // a contiguous range of units per cluster (at most one cluster per unit); both CTAs of a
+    // cluster take the same units
     const int64_t ncl = nclusters_x();
-    int chu = u < p.nunits ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
-    if (u < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chu), lu, tid, (int)kappa, 2);  // a hint
+    int64_t u = (int64_t)cluster_id_x() * p.nunits / ncl, lu = 0, lun = 0;
+    const int64_t uend = ((int64_t)cluster_id_x() + 1) * p.nunits / ncl;
+    int chu = u < uend ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
+    if (u < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chu), lu, tid, (int)kappa, 2);  // a hint
     if (warp == 0) {
         tmem_alloc(tm_slot, Q::TM_COLS);
         tmem_relinquish();
@@ -229,15 +232,15 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
-    if (u < p.nunits)  // phase A of the first unit
+    if (u < uend)  // phase A of the first unit
         pair_phase_c2a<REAL>(p, -1, nullptr, lu, chan<REAL>(p, chu), kappa, tlane, s, r, hi_s, wr_s, bufs);
-    for (; u < p.nunits; u += ncl) {
+    for (; u < uend; ++u) {
         tmem_fence_before_sync();
         __syncthreads();
         tmem_fence_after_sync();
-        const int64_t un = u + ncl;
-        const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
-        if (un < p.nunits && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, (int)kappa, 2);
+        const int64_t un = u + 1;
+        const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
+        if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, (int)kappa, 2);
         phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2);
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
         tmem_fence_before_sync();
         cluster_sync();  // the other CTA's P values have landed in bufs
         tmem_fence_after_sync();
-        pair_phase_c2a<REAL>(p, lu, chan<REAL>(p, chu).y, un < p.nunits ? lun : -1, chan<REAL>(p, chn), kappa, tlane,
+        pair_phase_c2a<REAL>(p, lu, chan<REAL>(p, chu).y, un < uend ? lun : -1, chan<REAL>(p, chn), kappa, tlane,
                              s, r, hi_s, wr_s, bufs);
         chu = chn;
         lu = lun;
