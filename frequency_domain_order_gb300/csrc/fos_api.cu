@@ -366,6 +366,13 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const void *func = channels > 1 && p->kernel.func_multi ? p->kernel.func_multi : p->kernel.func;
+    // less than one wave: each group filters one unit at most, so the per-thread Tensor Memory
+    // set-up of the plan constants would sit on the call's critical path; the variant that keeps
+    // them in shared memory avoids it
+    if (p->kernel.func_short && bp.nunits < (int64_t)p->max_units_in_flight * p->kernel.groups) {
+        func = p->kernel.func_short;
+        cfg.dynamicSmemBytes = (size_t)p->kernel.smem_short;
+    }
     FOS_CUDA(cudaLaunchKernelExC(&cfg, func, args), "block kernel launch");
     if (!bp.fuse_state && p->M > 1)
         FOS_CUDA(real ? launch_state<float>(x, n, state, p->M - 1, xs, ss, channels, stream)
@@ -561,6 +568,11 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
         if (p->kernel.func_multi) {
             e = cudaFuncSetAttribute(p->kernel.func_multi, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      p->kernel.smem);
+            if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
+        }
+        if (p->kernel.func_short) {
+            e = cudaFuncSetAttribute(p->kernel.func_short, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     p->kernel.smem_short);
             if (e != cudaSuccess) return bail(cuda_fail(e, "cudaFuncSetAttribute(smem)"));
         }
         if (p->kernel.cluster == 1) {

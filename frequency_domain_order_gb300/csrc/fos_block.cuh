@@ -70,8 +70,30 @@ struct BlockCfg {
         TM_NEED <= 32 ? 32 : TM_NEED <= 64 ? 64 : TM_NEED <= 128 ? 128 : TM_NEED <= 256 ? 256 : 512;
     static_assert(TM_NEED <= 512, "tensor memory columns");
     static_assert(THREADS % 128 == 0, "whole warp quarters");
+    // the variant for calls of less than one wave keeps H / N and the pass twiddles in shared
+    // memory after the buffers (no Tensor Memory): for N <= 1024 they fit beside them
+    static constexpr int SMC_BYTES = 8 * (N + S::TW_ENTRIES);
+    static constexpr bool HAS_SMC = SMEM_BYTES + SMC_BYTES <= 227 * 1024;
     using Bar = GroupBarrier<GT>;
 };
+
+// dst[0 .. n) = src[0 .. n) by the `threads` threads of the CTA, 16 bytes per load (plan tables
+// are 16-byte aligned), every load of a thread issued before its stores.
+__device__ __forceinline__ void copy_table(const float2 *src, float2 *dst, int n, int tid, int threads) {
+    const int n4 = n / 2;
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    for (int i0 = tid; i0 < n4; i0 += 4 * threads) {
+        float4 t[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i0 + q * threads < n4) t[q] = __ldg(s4 + i0 + q * threads);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i0 + q * threads < n4) d4[i0 + q * threads] = t[q];
+    }
+    if ((n & 1) && tid == 0) dst[n - 1] = __ldg(src + n - 1);
+}
 
 // Gather the input window of work unit u into `buf`.  Returns the element offset of
 // xt[start] inside the buffer.  A bulk copy is used (issued by thread 0, completing on
@@ -215,7 +237,9 @@ __device__ __forceinline__ void write_state(const BlockParams &p, const Chan &ch
     }
 }
 
-template <int LOGN, bool REAL>
+// SMC: H / N and the twiddles in shared memory instead of Tensor Memory (calls of less than one
+// wave, where the per-thread Tensor Memory set-up is on every call's critical path)
+template <int LOGN, bool REAL, bool SMC>
 __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, REAL>::MIN_BLOCKS)
     fos_block_kernel(const BlockParams p) {
     using C = BlockCfg<LOGN, REAL>;
@@ -237,7 +261,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     const typename C::Bar gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
-    if (warp == 0) {
+    if (!SMC && warp == 0) {
         tmem_alloc(tm_base_slot, C::TM_COLS);
         tmem_relinquish();
     }
@@ -272,9 +296,16 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     }
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
-    const uint32_t tma = *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
-                         (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
-    {
+    const uint32_t tma = SMC ? 0u
+                             : *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
+                                   (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+    float2 *cH = reinterpret_cast<float2 *>(smem + C::SMEM_BYTES);  // SMC: H / N, then the twiddles
+    float2 *cT = cH + C::N;
+    if constexpr (SMC) {
+        copy_table(p.H, cH, C::N, tid, C::THREADS);
+        copy_table(p.tw, cT, S::TW_ENTRIES, tid, C::THREADS);
+        __syncthreads();
+    } else {
         // H[j + e T] / N for e = 0..15, then the twiddles W_{16 Ns}^{(j mod Ns) r} of each pass;
         // every load is issued before the first store into TMEM
         float w[S::NPASS][32];
@@ -361,8 +392,11 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
         float2 *b1 = reinterpret_cast<float2 *>(cur) + f * xpad_len(C::N);
-        fft_tm<LOGN, 0, false>(v, b0, b1, nullptr, tma, j, gbar);
-        {
+        fft_tm<LOGN, SMC ? (1 << 30) : 0, false>(v, b0, b1, cT, tma, j, gbar);
+        if constexpr (SMC) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], cH[j + e * T]);
+        } else {
             float h[16];
             tmem_ld16(tma, h);
             tmem_wait_ld();
@@ -373,7 +407,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[8 + e] = cmul(v[8 + e], make_float2(h[2 * e], h[2 * e + 1]));
         }
-        fft_tm<LOGN, 0, true>(v, b0, b1, nullptr, tma, j, gbar);
+        fft_tm<LOGN, SMC ? (1 << 30) : 0, true>(v, b0, b1, cT, tma, j, gbar);
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
         const int64_t blk = REAL ? 2 * (lu * C::F + f) : (lu * C::F + f);
@@ -430,14 +464,18 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
-    if (warp == 0) tmem_dealloc(*tm_base_slot, C::TM_COLS);
+    if (!SMC && warp == 0) tmem_dealloc(*tm_base_slot, C::TM_COLS);
 }
 
 template <int LOGN, bool REAL>
 KernelEntry block_entry() {
     using C = BlockCfg<LOGN, REAL>;
     KernelEntry k;
-    k.func = reinterpret_cast<const void *>(&fos_block_kernel<LOGN, REAL>);
+    k.func = reinterpret_cast<const void *>(&fos_block_kernel<LOGN, REAL, false>);
+    if constexpr (C::HAS_SMC) {
+        k.func_short = reinterpret_cast<const void *>(&fos_block_kernel<LOGN, REAL, true>);
+        k.smem_short = C::SMEM_BYTES + C::SMC_BYTES;
+    }
     k.threads = C::THREADS;
     k.smem = C::SMEM_BYTES;
     k.cluster = 1;

@@ -64,6 +64,8 @@ __device__ __forceinline__ Chan chan(const BlockParams &p, int ch) {
 struct KernelEntry {
     const void *func = nullptr;  // __global__ function
     const void *func_multi = nullptr;  // the same for calls of more than one channel, if separate
+    const void *func_short = nullptr;  // the variant for calls of less than one wave, if any
+    int smem_short = 0;                // its dynamic shared memory per CTA (bytes)
     int threads = 0;             // threads per CTA
     int smem = 0;                // dynamic shared memory per CTA (bytes)
     int cluster = 1;             // CTAs per cluster (1 = no cluster)
