@@ -5,8 +5,9 @@
 // the state carry of step 3:
 //   gather   E_i = xt[i L - (M-1) .. i L - (M-1) + N) into shared memory.  Interior
 //            groups of blocks arrive by one bulk (TMA) copy issued while the previous group
-//            is being transformed (double-buffered); groups that touch the state S0 or run
-//            past the input are gathered with plain loads (S0 in front, zeros behind).
+//            is being transformed (double-buffered); for groups that touch the state S0 or run
+//            past the input, the part inside x comes by bulk copy and the rest (S0 in front,
+//            the ragged ends, zeros behind) by plain loads.
 //   FFT      F_i = FFT_N(E_i) in registers and two alternating exchange buffers
 //   multiply I_i = F_i * H
 //   IFFT     R_i = IFFT_N(I_i), natural order in registers
@@ -20,18 +21,22 @@
 // Per-thread constants -- the 16 bins of H / N a thread multiplies and the twiddles of its
 // passes -- are written once into Tensor Memory (this thread's lane) and read back with
 // tcgen05.ld for every block, keeping them off the shared-memory / L1 path that carries the
-// exchanges.  Each group's shared memory holds three buffers: two staging windows (the one being filtered
-// and the one being fetched) and one exchange buffer; the window being filtered doubles as
-// the second exchange buffer once it has been read.
+// exchanges.  A call of less than one wave (each group one unit at most) runs the SMC variant
+// instead (N <= 1024): the tables sit in shared memory beside the buffers, one coalesced copy
+// per CTA, which takes the Tensor Memory set-up off the call's critical path.  Each group's
+// shared memory holds three buffers: two staging windows (the one being filtered and the one
+// being fetched) and one exchange buffer; the window being filtered doubles as the second
+// exchange buffer once it has been read.
 //
 // A CTA that allocates Tensor Memory runs alone on its SM, so a CTA has 512 threads split
 // into independent groups of max(64, N/16) threads (eight groups for N <= 1024, two for
 // N = 4096, one for N = 8192), each with its own three buffers, mbarriers and hardware barrier,
-// sharing only the Tensor Memory allocation.  Grid: persistent, one CTA per SM; the groups of
-// all CTAs take work units round-robin.  A work unit is F consecutive blocks (complex) or F
-// consecutive block pairs (real), F = max(1, 64 / (N/16)), each handled by N/16 threads: small
-// transforms spread over as many groups as possible, so that a call of few blocks finishes in
-// the time of one unit.
+// sharing only the Tensor Memory allocation.  Grid: persistent, one CTA per SM; a call of
+// fewer units than groups deals them across CTAs first, a longer one gives each CTA a
+// contiguous range of units that its groups take in turn.  A work unit is F consecutive blocks
+// (complex) or F consecutive block pairs (real), F = max(1, 64 / (N/16)), each handled by N/16
+// threads: small transforms spread over as many groups as possible, so that a call of few
+// blocks finishes in the time of one unit.
 #pragma once
 
 #include <type_traits>
