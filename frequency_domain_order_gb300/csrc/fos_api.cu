@@ -410,28 +410,28 @@ struct BlockCost {
     double sm_us[3];  // at L/N = 1/4, 1/2, 3/4
 };
 const BlockCost kBlockCost[] = {
-    {64, 0, {0.0316, 0.0342, 0.0376}},
-    {128, 0, {0.0479, 0.0509, 0.0547}},
-    {256, 0, {0.0897, 0.0942, 0.1003}},
-    {512, 0, {0.2401, 0.2492, 0.2599}},
-    {1024, 0, {0.4956, 0.5105, 0.5334}},
-    {2048, 0, {1.1095, 1.1425, 1.1851}},
-    {4096, 0, {2.4438, 2.5772, 2.6979}},
-    {8192, 0, {6.6633, 7.0034, 7.5149}},
-    {16384, 0, {14.8344, 16.0482, 17.3649}},
-    {32768, 0, {28.8420, 31.9048, 36.4983}},
-    {65536, 0, {81.4112, 89.4854, 100.4466}},
-    {64, 1, {0.0205, 0.0228, 0.0261}},
-    {128, 1, {0.0281, 0.0302, 0.0325}},
-    {256, 1, {0.0479, 0.0509, 0.0539}},
-    {512, 1, {0.1229, 0.1292, 0.1368}},
-    {1024, 1, {0.2538, 0.2622, 0.2780}},
-    {2048, 1, {0.5916, 0.6034, 0.6336}},
-    {4096, 1, {1.4052, 1.4833, 1.5716}},
-    {8192, 1, {3.3590, 3.5340, 3.8174}},
-    {16384, 1, {7.4628, 8.2924, 9.1146}},
-    {32768, 1, {15.4310, 17.4253, 20.7923}},
-    {65536, 1, {43.0190, 47.4605, 53.7230}},
+    {64, 0, {0.0315, 0.0340, 0.0370}},
+    {128, 0, {0.0472, 0.0501, 0.0535}},
+    {256, 0, {0.0870, 0.0912, 0.0968}},
+    {512, 0, {0.2358, 0.2461, 0.2554}},
+    {1024, 0, {0.4808, 0.5014, 0.5196}},
+    {2048, 0, {1.0836, 1.1166, 1.1668}},
+    {4096, 0, {2.4637, 2.5038, 2.6723}},
+    {8192, 0, {6.5200, 6.9616, 7.4397}},
+    {16384, 0, {14.7463, 16.0497, 17.3581}},
+    {32768, 0, {28.5274, 31.8075, 36.5530}},
+    {65536, 0, {78.5992, 82.8704, 92.8540}},
+    {64, 1, {0.0204, 0.0226, 0.0256}},
+    {128, 1, {0.0274, 0.0296, 0.0320}},
+    {256, 1, {0.0468, 0.0494, 0.0524}},
+    {512, 1, {0.1193, 0.1246, 0.1310}},
+    {1024, 1, {0.2464, 0.2557, 0.2689}},
+    {2048, 1, {0.6023, 0.6139, 0.6199}},
+    {4096, 1, {1.2270, 1.2844, 1.3675}},
+    {8192, 1, {3.3370, 3.5279, 3.7678}},
+    {16384, 1, {7.3716, 8.2430, 9.0462}},
+    {32768, 1, {15.2068, 17.3128, 20.4274}},
+    {65536, 1, {42.8199, 45.2291, 51.0948}},
 };
 
 // Predicted throughput (output samples per second, 1e9) of an (M, N) plan on `sms` SMs: L
