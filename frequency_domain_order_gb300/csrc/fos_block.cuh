@@ -194,9 +194,9 @@ __device__ __forceinline__ int stage_unit(const BlockParams &p, const Chan &ch, 
 }
 
 // Prefetch into L2 the part of unit u's window that lies in x (rounded inwards to 16 bytes),
-// one instruction issued by thread 0 of the group (issuing costs time; the window is small).  A prefetch makes nothing visible to this
-// kernel, so it may run before the wait for the kernel before it: the later gather still reads
-// whatever that kernel wrote.
+// one instruction issued by thread 0 of the group (issuing costs time; the window is small).
+// A prefetch makes nothing visible to this kernel, so it may run before the wait for the
+// kernel before it: the later gather still reads whatever that kernel wrote.
 template <int LOGN, bool REAL>
 __device__ __forceinline__ void prefetch_unit(const BlockParams &p, const Chan &ch, int64_t u, int tid) {
     using C = BlockCfg<LOGN, REAL>;
