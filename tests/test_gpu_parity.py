@@ -107,6 +107,32 @@ def test_shards_with_halos_equal_one_call(name, blocks, tail, parts):
     assert np.array_equal(st1.cpu().numpy(), last.cpu().numpy())
 
 
+@pytest.mark.parametrize("name", ["C4", "C1"])
+def test_short_call_variant_equals_full_wave(name):
+    """Calls of less than one wave (N <= 1024) run the kernel variant that keeps H and the
+    twiddles in shared memory; longer calls keep them in Tensor Memory.  The same stream filtered
+    in one call of about 2.5 waves and in calls of under one wave each (split on whole
+    transforms) gives the same output and state bit for bit."""
+    torch = pytest.importorskip("torch")
+    base = W.WORKLOADS[name]
+    plan = make_plan(base)
+    groups = 512 // max(64, base.N // 16)
+    per_unit = max(1, 64 // (base.N // 16)) * (2 if base.real else 1)  # blocks per work unit
+    wave = plan.kernel()["grid"] * groups * per_unit  # blocks in one wave of units
+    span = base.L * (2 if base.real else 1)
+    w = W.scaled(base, (5 * wave) // 2, 0)
+    x = W.make_x(w)
+    s0 = W.make_x(W.scaled(base, 1))[: base.M - 1]
+    xd = to_dev(x)
+    y1, st1 = run_device(plan, xd, (w.n,), to_dev(s0))
+    chunk = (wave * base.L * 2 // 3) // span * span  # two thirds of a wave, whole transforms
+    calls = [chunk] * (w.n // chunk) + ([w.n % chunk] if w.n % chunk else [])
+    y2, st2 = run_device(plan, xd, calls, to_dev(s0))
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), y2.cpu().numpy().view(np.uint32))
+    assert np.array_equal(st1.cpu().numpy(), st2.cpu().numpy())
+    plan.close()
+
+
 # ----------------------------------------------------------------------------- full size, sampled
 
 
