@@ -103,12 +103,13 @@ _NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_p
 
 
 class ClockSampler:
-    """Reads SM clocks and clock-event reasons through NVML (read-only queries) every
-    `period` seconds on a background thread while the timed region runs."""
+    """Reads SM and memory clocks and clock-event reasons through NVML (read-only queries)
+    every `period` seconds on a background thread while the timed region runs."""
 
     def __init__(self, device_index: int, period: float = 0.002):
         self.ok = False
         self.samples = []
+        self.mem_samples = []
         self.reasons = 0
         self.period = period
         try:
@@ -127,6 +128,8 @@ class ClockSampler:
             mx = ctypes.c_uint()
             self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
             self.max_mhz = int(mx.value)
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 2, ctypes.byref(mx))  # 2: memory clock
+            self.mem_max_mhz = int(mx.value)
             self.ok = True
         except OSError:
             return
@@ -144,6 +147,9 @@ class ClockSampler:
         clk = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
         self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        mem = ctypes.c_uint()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 2, ctypes.byref(mem))
+        self.mem_samples.append(int(mem.value))
         f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
         f(self.h, ctypes.byref(rs))
@@ -172,6 +178,8 @@ class ClockSampler:
         if not self.ok or not self.samples:
             return None
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "mem_mhz": statistics.median(self.mem_samples) if self.mem_samples else None,
+                "mem_max_mhz": self.mem_max_mhz,
                 "samples": len(self.samples),
                 "reasons": [n for b, n in _NVML_REASONS.items() if self.reasons & b and b != 0x1],
                 "source": "NVML, sampled every 2 ms during the timed region"}
