@@ -22,7 +22,9 @@ claim steps 1-6: an M-tap h, FFT size N, block length L = N - M + 1):
 
 Random numbers: numpy Generator(PCG64(seed)).  A complex signal draws all real parts,
 then all imaginary parts, in float64, then is rounded to complex64; the oracle is fed
-the rounded values, so both sides see bit-identical inputs.
+the rounded values, so both sides see bit-identical inputs.  Streams past 2^31 samples are
+drawn on the device by torch's seeded generator instead (device_signal); the oracle gets
+copies of the windows it needs.
 """
 from __future__ import annotations
 
@@ -112,6 +114,19 @@ def uniform_real(n: int, seed: int) -> np.ndarray:
     """n real samples uniform in [-1, 1), float64."""
     rng = np.random.Generator(np.random.PCG64(seed))
     return rng.uniform(-1.0, 1.0, n)
+
+
+def device_signal(n: int, real: bool, seed: int, device: str = "cuda"):
+    """n input samples drawn on the device by torch's seeded generator, for streams too long to
+    draw on the host (past 2^31 samples): float32 uniform in [-1, 1), or complex64 whose re
+    and im are each N(0, 1/2).  Returns a torch tensor; windows of it are copied to the host
+    for the oracle."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    if real:
+        return torch.rand(n, generator=g, device=device, dtype=torch.float32).mul_(2.0).sub_(1.0)
+    return torch.randn(n, generator=g, device=device, dtype=torch.complex64)
 
 
 # ----------------------------------------------------------------------------- workloads
