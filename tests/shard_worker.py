@@ -3,7 +3,7 @@ torch.distributed.run with the gloo backend, on the CPU).
 
 Each rank filters its shard of a small stream with the float64 oracle, using its halo as the
 state; the ranks gather their outputs and final states, and rank 0 checks them against one
-oracle call over the whole stream and writes the verdict to the JSON file named on the command
+oracle call over the whole stream and writes the result to the JSON file named on the command
 line.  The step-time reduction of bench.py (max over ranks) is exercised with the same group.
 """
 import json
@@ -25,7 +25,7 @@ from frequency_domain_order_gb300.shard import halo, shard_ranges  # noqa: E402
 def main(out_path: str) -> int:
     dist.init_process_group("gloo")
     rank, world = dist.get_rank(), dist.get_world_size()
-    verdict = {}
+    result = {}
     for name in ("C1", "C4"):
         w = W.WORKLOADS[name]
         if name == "C4":
@@ -41,17 +41,17 @@ def main(out_path: str) -> int:
         if rank == 0:
             y1, s1 = oracle.direct(x, h, s0)
             ys = np.concatenate([p[2] for p in sorted(parts, key=lambda t: t[0])])
-            verdict[name] = {
+            result[name] = {
                 "ranges": [list(p[:2]) for p in parts],
                 "outputs_equal": bool(np.array_equal(ys, y1)),
                 "state_equal": bool(np.array_equal(parts[-1][3], s1)),
             }
     # bench.py's timing reduction over ranks
-    verdict["reduce_max"] = bench.reduce_max(float(rank + 1), world, "cpu")
+    result["reduce_max"] = bench.reduce_max(float(rank + 1), world, "cpu")
     bench.barrier(world)
     if rank == 0:
         with open(out_path, "w") as f:
-            json.dump(verdict, f)
+            json.dump(result, f)
     dist.destroy_process_group()
     return 0
 

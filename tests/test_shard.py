@@ -76,7 +76,7 @@ def _free_port() -> int:
 
 
 def test_two_gloo_ranks_filter_one_stream(tmp_path):
-    out = tmp_path / "verdict.json"
+    out = tmp_path / "result.json"
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr=127.0.0.1", f"--master-port={_free_port()}",
            os.path.join(ROOT, "tests", "shard_worker.py"), str(out)]
