@@ -190,6 +190,24 @@ def pin_overlap_save_matches_definition(o):
         assert np.array_equal(s_os, np.concatenate([s, x])[-(M - 1):] if M > 1 else s_os)
 
 
+def pin_overlap_save_with_any_response(o):
+    """With a response that is not the transform of an M-tap h (random bins), steps 2-5
+    give, block by block, the kept part of a circular convolution: R_i[M-1 .. M-1+L) with
+    R_i = IDFT(DFT(E_i) H), E_i = xt[i L - (M-1) .. i L - (M-1) + N), computed here with
+    numpy's FFT on the extended input (state in front, zeros past x)."""
+    rng = _rng(23)
+    for M, N, n in [(7, 16, 45), (67, 256, 3 * 190 + 31), (1, 8, 13), (16, 16, 5)]:
+        H = _cn(rng, N)
+        x, s = _cn(rng, n), _cn(rng, M - 1)
+        L = N - M + 1
+        k = (n + L - 1) // L
+        xt = np.concatenate([s, x, np.zeros(k * L + N)])
+        want = np.concatenate([np.fft.ifft(np.fft.fft(xt[i * L: i * L + N]) * H)[M - 1: M - 1 + L]
+                               for i in range(k)])[:n] if n else np.zeros(0, complex)
+        y_os, _ = o.overlap_save(x, H, M, s)
+        assert np.allclose(y_os, want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max())), (M, N, n)
+
+
 def pin_given_response_is_causal(o):
     """A response given as complex64 (the FFT of an M-tap h, rounded) inverts, through the
     oracle's own inverse FFT, to h below M and to ~0 from M on."""
@@ -288,7 +306,7 @@ ALL_PINS = [
     pin_golden_tiny, pin_impulse, pin_step, pin_numpy_convolve, pin_exponential_eigen,
     pin_linearity_and_shift, pin_split_stream, pin_direct_at, pin_dft_textbook,
     pin_fft_library, pin_freq_response, pin_overlap_save_matches_definition,
-    pin_given_response_is_causal,
+    pin_overlap_save_with_any_response, pin_given_response_is_causal,
     pin_chan_tone, pin_chan_impulse, pin_chan_single_channel_is_convolution, pin_chan_hop_invariant,
     pin_chan_split_stream,
 ]

@@ -302,6 +302,38 @@ def test_given_response_matches_taps(N, M, real):
     assert_parity(yf[idx], want.real if real else want, h64, x, "given H")
 
 
+@pytest.mark.parametrize("N,real", [(256, False), (1024, True), (4096, False), (4096, True), (32768, False),
+                                    (65536, False)])
+def test_given_response_without_taps(N, real):
+    """A given response that is not the transform of an M-tap filter (random bins, Hermitian
+    for real data): every block is then a circular convolution with h_eff = IDFT(H), of which
+    step 5 keeps R_i[M-1 .. M-1+L).  The oracle runs steps 2-5 block by block with the same
+    H; the bar takes ||h_eff||_1 in place of ||h||_1.  Unlike a linear convolution, the result
+    now depends on where the blocks start, so the stream is cut into calls at a multiple of L
+    (a call's blocks start at its first sample)."""
+    from frequency_domain_order_gb300 import fir_os
+    rng = np.random.default_rng(7000 + N + real)
+    M = N // 4 + 3
+    L = N - M + 1
+    n = 3 * L + L // 2 + 5
+    G = rng.standard_normal(N) + 1j * rng.standard_normal(N)
+    if real:
+        G = 0.5 * (G + np.conj(G[(-np.arange(N)) % N]))  # Hermitian: h_eff is real
+        x = rng.uniform(-1, 1, n).astype(np.float32)
+        s0 = rng.uniform(-1, 1, M - 1).astype(np.float32)
+    else:
+        x = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
+        s0 = (rng.standard_normal(M - 1) + 1j * rng.standard_normal(M - 1)).astype(np.complex64)
+    H = G.astype(np.complex64)
+    plan = fir_os.Plan(M, N, to_dev(H), real=real, coef_kind=fir_os.COEF_FREQ)
+    cut = 2 * L
+    y, st = run_calls(plan, x, (cut, n - cut), s0)
+    want, s_want = oracle.overlap_save(x, H, M, s0)
+    h_eff = np.fft.ifft(H.astype(np.complex128))
+    assert_parity(y, want.real if real else want, h_eff, x, f"N={N} real={real} given H")
+    assert np.array_equal(st, s_want.real.astype(st.dtype) if real else s_want.astype(st.dtype))
+
+
 # ----------------------------------------------------------------------------- host buffers
 
 
