@@ -239,6 +239,23 @@ namespace {
 
 int sample_bytes(const fir_os_plan *p) { return p->data_kind == FIR_OS_REAL ? 4 : 8; }
 
+// Makes `dev` the current device for the lifetime of the object and then restores the
+// caller's current device (plans are destroyed on the device that holds their memory).
+struct DeviceScope {
+    int prev = -1;
+    explicit DeviceScope(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            cudaGetLastError();
+            prev = -1;
+        } else if (prev != dev) {
+            cudaSetDevice(dev);
+        }
+    }
+    ~DeviceScope() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
 void free_plan(fir_os_plan *p) {
     if (!p) return;
     cudaFree(p->d_H);
@@ -704,6 +721,7 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
 
 int fir_os_plan_destroy(fir_os_plan_t plan) {
     if (!plan) return FIR_OS_OK;
+    DeviceScope on(plan->device);
     cudaDeviceSynchronize();
     free_plan(plan);
     return FIR_OS_OK;
@@ -948,6 +966,7 @@ struct fir_chan_plan {
 
 int fir_chan_plan_destroy(fir_chan_plan_t plan) {
     if (!plan) return FIR_OS_OK;
+    DeviceScope on(plan->device);
     cudaDeviceSynchronize();
     cudaFree(plan->d_h);
     cudaFree(plan->d_tw);

@@ -157,8 +157,8 @@ int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n_sample
  * performs (two per multiply-add).  FIR_OS_E_INVAL for iters < 1 or flops NULL. */
 int fir_os_fp32_probe(int iters, void *stream, double *flops);
 
-/* fir_os_plan_destroy -- synchronises the device work of the plan and frees it. NULL is a
- * no-op. */
+/* fir_os_plan_destroy -- synchronises the plan's device (made current for the call; the
+ * caller's current device is restored) and frees the plan.  NULL is a no-op. */
 int fir_os_plan_destroy(fir_os_plan_t plan);
 
 /* fir_os_plan_info -- M, N and L = N - M + 1 of a plan (any output pointer may be NULL). */
@@ -269,7 +269,8 @@ int fir_chan_execute(fir_chan_plan_t plan, const void *x, int64_t n_samples, voi
 /* fir_chan_plan_info -- K, D and Nh of a channelizer plan (any output may be NULL). */
 int fir_chan_plan_info(fir_chan_plan_t plan, int *K, int *D, int *Nh);
 
-/* fir_chan_plan_destroy -- synchronises the device and frees the plan.  NULL is a no-op. */
+/* fir_chan_plan_destroy -- synchronises the plan's device (made current for the call; the
+ * caller's current device is restored) and frees the plan.  NULL is a no-op. */
 int fir_chan_plan_destroy(fir_chan_plan_t plan);
 
 /* fir_os_status_string -- a static description of a status code. */
