@@ -196,9 +196,11 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     using Q = PairCfg<REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int s = tid >> 7, r = tid & 127;
-    const int g = tid >> 8, j = tid & 255;
+    // the warp index broadcast from lane 0, so that the compiler knows it (and s, g, the Tensor
+    // Memory addresses derived from it) to be the same in every lane of a warp
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const int s = warp >> 2, r = tid & 127;  // phases A and C: s = tid / 128
+    const int g = warp >> 3, j = tid & 255;  // phase B: g = tid / 256
     const uint32_t kappa = cluster_ctarank();
     uint32_t *tm_slot = reinterpret_cast<uint32_t *>(smem);
     float2 *stw = reinterpret_cast<float2 *>(smem + Q::OFF_TW);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     tmem_fence_before_sync();
     cluster_sync();  // both CTAs are running (and set up) before any remote store
     tmem_fence_after_sync();
-    const uint32_t tlane = *tm_slot + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
         const int64_t un = u + 1;
         const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, (int)kappa, 2);
-        phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2);
+        phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2, 32u * (uint32_t)((warp >> 2) & 1));
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
         tmem_fence_after_sync();

@@ -144,9 +144,11 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     using R_ = ResidentCfg<LOGN, REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int s = tid >> 7, r = tid & 127;  // phases A and C
-    const int g = tid >> 8, j = tid & 255;  // phase B
+    // the warp index broadcast from lane 0, so that the compiler knows it (and s, g, the Tensor
+    // Memory addresses derived from it) to be the same in every lane of a warp
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const int s = warp >> 2, r = tid & 127;  // phases A and C: s = tid / 128
+    const int g = warp >> 3, j = tid & 255;  // phase B: g = tid / 256
     uint32_t *tm_slot = reinterpret_cast<uint32_t *>(smem);
     float2 *stw = reinterpret_cast<float2 *>(smem + R_::OFF_TW);
     float2 *hi_s = reinterpret_cast<float2 *>(smem + R_::OFF_HI);
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
-    const uint32_t tlane = *tm_slot + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
         const int64_t un = u + gridDim.x;
         const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, chan<REAL>(p, chn), lun, tid);
-        phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1);
+        phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();

@@ -78,13 +78,12 @@ __device__ __forceinline__ void prefetch_window(const BlockParams &p, const Chan
 
 // Phase B: P-point FFT, multiply by H, inverse FFT for the CL local sub-transforms
 // c' = g, g + 2, ... (Tensor Memory columns 64 c'), whose bins are H[c + C d] with
-// c = hoff + hstride c'.
+// c = hoff + hstride c'.  col0 = 32 (j >> 7), passed in by the caller as a warp-uniform value.
 template <int CL>
 __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
                                         float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar, int hoff,
-                                        int hstride) {
+                                        int hstride, uint32_t col0) {
     constexpr int LOGP = 12, P = 1 << LOGP;
-    const uint32_t col0 = 32u * (uint32_t)(j >> 7);
 #pragma unroll 1
     for (int c = g; c < CL; c += 2) {
         const uint32_t ta = tlane + 64u * (uint32_t)c + col0;
