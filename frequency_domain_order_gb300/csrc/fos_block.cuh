@@ -54,6 +54,7 @@ struct BlockCfg {
     static constexpr int F = T >= 64 ? 1 : 64 / T;
     static constexpr int GT = F * T;              // threads of one group: max(64, N / 16)
     static constexpr int GROUPS = 512 / GT;       // independent groups per CTA (8 .. 1)
+    static_assert(GT % 32 == 0, "whole warps per group");
     static constexpr int THREADS = 512;
     static constexpr int SB = REAL ? 4 : 8;  // bytes per sample
     // F blocks' gather windows (complex: (F-1)L + N samples; real: (2F-1)L + N floats) fit in
@@ -252,8 +253,10 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     constexpr int T = C::T;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int g = tid / C::GT;      // group within the CTA
+    // the warp index broadcast from lane 0, so that the compiler knows it (and the group, the
+    // Tensor Memory addresses derived from it) to be the same in every lane of a warp
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const int g = warp / (C::GT / 32);  // group within the CTA (GT is a multiple of 64)
     const int tg = tid % C::GT;     // thread within the group
     const int f = tg / T;           // transform slot within the group
     const int j = tg % T;           // thread within the transform
@@ -302,8 +305,8 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
     const uint32_t tma = SMC ? 0u
-                             : *tm_base_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
-                                   (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+                             : __shfl_sync(0xffffffffu, *tm_base_slot, 0) +
+                                   ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
     float2 *cH = reinterpret_cast<float2 *>(smem + C::SMEM_BYTES);  // SMC: H / N, then the twiddles
     float2 *cT = cH + C::N;
     if constexpr (SMC) {
