@@ -137,10 +137,7 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
         const int b = r + 128 * m;
         const uint32_t col = 2u * (uint32_t)(16 * (m & 1) + (m >> 1));  // slot (0, m); + 64 per a' or c'
         float2 x[16];
-        if (ua >= 0) {
-#pragma unroll
-            for (int a = 0; a < 16; ++a) x[a] = load_point<REAL>(p, cha, sa + P * a + b, interior);
-        }
+        if (ua >= 0) load_points<REAL, 16, P>(p, cha, sa + b, interior, x);
         if (q < 4 && uc >= 0) {
             float2 pown[8];
 #pragma unroll

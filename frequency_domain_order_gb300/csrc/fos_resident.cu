@@ -92,8 +92,7 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int b = r + 128 * (8 * s + i0 + 2 * h);
-#pragma unroll
-                for (int a = 0; a < C; ++a) xa[h][a] = load_point<REAL>(p, cha, sa + P * a + b, interior);
+                load_points<REAL, C, P>(p, cha, sa + b, interior, xa[h]);
             }
         }
         if (uc >= 0) {

@@ -47,6 +47,28 @@ __device__ __forceinline__ float2 load_point(const BlockParams &p, const Chan &c
     }
 }
 
+// v[a] = xt[t0 + P a] for a < NA (load_point of each), with the test for a window that lies
+// inside x taken once: there every point is a plain load at a constant offset from one pointer.
+template <bool REAL, int NA, int P>
+__device__ __forceinline__ void load_points(const BlockParams &p, const Chan &ch, int64_t t0, bool interior,
+                                            float2 (&v)[NA]) {
+    if (interior) {
+        if constexpr (REAL) {
+            const float *x = static_cast<const float *>(ch.x) + t0;
+            const float *x2 = x + p.L;
+#pragma unroll
+            for (int a = 0; a < NA; ++a) v[a] = make_float2(x[P * a], x2[P * a]);
+        } else {
+            const float2 *x = static_cast<const float2 *>(ch.x) + t0;
+#pragma unroll
+            for (int a = 0; a < NA; ++a) v[a] = x[P * a];
+        }
+    } else {
+#pragma unroll
+        for (int a = 0; a < NA; ++a) v[a] = load_point<REAL>(p, ch, t0 + (int64_t)P * a, false);
+    }
+}
+
 // Bulk L2 prefetch of part `part` of `parts` of the input window of unit u of channel ch (the
 // part of the window inside x), split over 128 threads (pieces of ~2 KB: a few large prefetches
 // are fetched far slower than many small ones, measured 1 / 16 / 32 / 128 pieces).
