@@ -125,6 +125,8 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
     const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
     const bool whole = sc + Q::N + (REAL ? p.L : 0) <= p.n;
     const int keep = p.M - 1;
+    // outputs R[t] of unit uc with t < lim exist (t < N, so lim is capped to an int)
+    const int lim = p.n - sc > (int64_t)Q::N + p.L ? Q::N + p.L : (int)(p.n - sc);
     const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
     const bool interior = sa >= 0 && sa + Q::N + (REAL ? p.L : 0) <= p.n;
     float2 wr[8];
@@ -154,14 +156,14 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
                     const float2 val = h == 0 ? cadd(p0, w) : csub(p0, w);
                     const int t = P * (a + 8 * h) + b;
                     if (t < keep) continue;
-                    const int64_t o = sc + t;
+                    // y[sc + b + P (a + 8 h)] at a constant offset from one pointer
                     if constexpr (REAL) {
-                        float *y = static_cast<float *>(yc);
-                        if (whole || o < p.n) st_cs(y + o, val.x);
-                        if (whole || o + p.L < p.n) st_cs(y + o + p.L, val.y);
+                        float *yb = static_cast<float *>(yc) + sc + b;
+                        if (whole || t < lim) st_cs(yb + P * (a + 8 * h), val.x);
+                        if (whole || t + p.L < lim) st_cs(yb + p.L + P * (a + 8 * h), val.y);
                     } else {
-                        float2 *y = static_cast<float2 *>(yc);
-                        if (whole || o < p.n) st_cs(y + o, val);
+                        float2 *yb = static_cast<float2 *>(yc) + sc + b;
+                        if (whole || t < lim) st_cs(yb + P * (a + 8 * h), val);
                     }
                 }
             }

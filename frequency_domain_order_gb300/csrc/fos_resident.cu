@@ -78,6 +78,8 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
     const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
     const bool whole = sc + R_::N + (REAL ? p.L : 0) <= p.n;
     const int keep = p.M - 1;
+    // outputs R[t] of unit uc with t < lim exist (t = P a + b < N, so lim is capped to an int)
+    const int lim = p.n - sc > (int64_t)R_::N + p.L ? R_::N + p.L : (int)(p.n - sc);
     const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
     const bool interior = sa >= 0 && sa + R_::N + (REAL ? p.L : 0) <= p.n;
     float2 wr[C];
@@ -107,18 +109,18 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
                 for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
                 dft<C, +1>(v[h]);
                 const int b = r + 128 * m;
+                // y[sc + b + P a] at a constant offset from one pointer (dereferenced only for t >= keep)
 #pragma unroll
                 for (int a = 0; a < C; ++a) {
                     const int t = P * a + b;
                     if (t < keep) continue;
-                    const int64_t o = sc + t;
                     if constexpr (REAL) {
-                        float *y = static_cast<float *>(yc);
-                        if (whole || o < p.n) st_cs(y + o, v[h][a].x);
-                        if (whole || o + p.L < p.n) st_cs(y + o + p.L, v[h][a].y);
+                        float *yb = static_cast<float *>(yc) + sc + b;
+                        if (whole || t < lim) st_cs(yb + P * a, v[h][a].x);
+                        if (whole || t + p.L < lim) st_cs(yb + p.L + P * a, v[h][a].y);
                     } else {
-                        float2 *y = static_cast<float2 *>(yc);
-                        if (whole || o < p.n) st_cs(y + o, v[h][a]);
+                        float2 *yb = static_cast<float2 *>(yc) + sc + b;
+                        if (whole || t < lim) st_cs(yb + P * a, v[h][a]);
                     }
                 }
             }
