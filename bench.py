@@ -2,13 +2,17 @@
 
 One step is one pass of the whole hot path -- the fused block kernel over one call's input
 (steps 3-5 of the overlap-save claim in "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法",
-zl.czvv.com/42398539.html, plus the state carry) -- for the chosen workload (default C2:
-complex64, k = 4096 blocks of L = 3073, M = 1024, N = 4096, one call).  The C4 workload's step
-is its stream of 64 calls.
+zl.czvv.com/42398539.html, plus the state carry) -- for the chosen workload (default C5, the largest single-GPU
+workload: complex64, k = 2048 blocks of L = 49152, N = 65536 with the response H given, one
+call).  The C4 workload's step is its stream of 64 calls.  With the default workload the line
+also carries, under "also", the same measurement of C3 (k = 1024 blocks of L = 24577,
+N = 32768), the other long-transform workload.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C5] [--also C3,...]
+                  [--blocks B] [--impl ours|reference]
 
-Prints one JSON line on rank 0.  Under torchrun rank g filters shard g of one stream of N
+`--blocks B` shortens a single-call workload to B blocks (for profiler captures of a smaller
+case of the same kernel).  Prints one JSON line on rank 0.  Under torchrun rank g filters shard g of one stream of N
 workload-sized shards on its own GPU, its state starting as the halo (the last M-1 samples of
 shard g-1) -- weak scaling, no data-path collective -- and the time is the maximum over ranks.  `--impl reference` times the float64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload.
@@ -17,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -324,8 +329,27 @@ def config_block(w: W.Workload, footprint: int, sets: int = 2):
     }
 
 
-def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
+def plan_time(fir_os, w: W.Workload, coef, kind, reps: int = 5):
+    """Wall time of fir_os_plan_create (device allocations, step 1 -- the frequency response, or
+    the scaling and reordering of a given H -- and the final synchronisation), median of `reps`
+    plans created after the first."""
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        p = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=kind)
+        times.append((time.perf_counter() - t0) * 1e3)
+        p.close()
+    return {"median": statistics.median(times), "min": min(times), "reps": reps,
+            "what": ("fir_os_plan_create wall time: device allocations, step 1 "
+                     + ("(scaling and reordering of the given H)" if kind == fir_os.COEF_FREQ else
+                        "(float64 FFT of the taps on the device, rounded once)")
+                     + ", synchronised; median of plans created after a first")}
+
+
+def run_ours(args, w: W.Workload, world: int, rank: int, local: int, cpu_budget: float = None):
     import torch
+    if cpu_budget is None:
+        cpu_budget = args.cpu_budget
 
     from frequency_domain_order_gb300 import build as fbuild
     from frequency_domain_order_gb300 import fir_os
@@ -334,7 +358,8 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
     dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
     if rank == 0 or not os.path.exists(fbuild.LIB):
         fbuild.build()
     barrier(world)
@@ -352,10 +377,12 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
         halo = np.zeros((w.channels, w.M - 1), dtype=x.dtype)
     if w.coef == "freq":
         coef = torch.from_numpy(W.make_H_given(w)).to(dev)
-        plan = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=fir_os.COEF_FREQ)
+        kind = fir_os.COEF_FREQ
     else:
         coef = torch.from_numpy(W.make_h_device(w)).to(dev)
-        plan = fir_os.Plan(w.M, w.N, coef, real=w.real)
+        kind = fir_os.COEF_TIME
+    plan = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=kind)
+    plan_ms = plan_time(fir_os, w, coef, kind)
     sets = buffer_sets(2 * x.nbytes)
     xs = [torch.from_numpy(x).to(dev) for _ in range(sets)]
     ys = [torch.empty_like(xs[0]) for _ in range(sets)]
@@ -515,13 +542,14 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int):
                         if graphs is not None else "direct launches"),
         "clocks": clk,
         "kernel": plan.kernel(),
+        "plan_ms": plan_ms,
         "wall_s_timed_region": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # (a bank of channels: the oracle on channel 0, the same per-sample work)
         x0 = x if w.channels == 1 else x[0]
-        out["cpu_baseline"] = cpu_baseline(w, x0, budget_s=args.cpu_budget)
-        pc = single_thread_overlap_save(w, x0, budget_s=min(3.0, args.cpu_budget))
+        out["cpu_baseline"] = cpu_baseline(w, x0, budget_s=cpu_budget)
+        pc = single_thread_overlap_save(w, x0, budget_s=min(3.0, cpu_budget))
         pc["gpu_over_cpu"] = out["value"] / pc["value"]
         out["page_comparison"] = pc
     plan.close()
@@ -814,13 +842,34 @@ def run_chan_reference(args, c, world: int, rank: int):
 # ----------------------------------------------------------------------------- main
 
 
+DEFAULT_CONFIG = "C5"
+DEFAULT_ALSO = ["C3"]
+ALSO_KEYS = ("value", "unit", "ms_per_step", "ms_per_step_median", "ms_per_step_p20", "config", "roofline",
+             "fp32", "metric_roofline", "e2e", "gpu_launches", "launch_mode", "clocks", "kernel", "plan_ms",
+             "cpu_baseline", "page_comparison")
+
+
+def workload(name: str, blocks: int = 0) -> W.Workload:
+    """A workload by name; with blocks > 0 a single-call workload shortened to that many blocks."""
+    w = W.WORKLOADS[name]
+    if blocks > 0 and len(w.calls) == 1:
+        w = dataclasses.replace(W.scaled(w, blocks),
+                                description=f"{w.description}, shortened to k={blocks} blocks")
+    return w
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS) + sorted(W.CHANNELIZERS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(W.WORKLOADS) + sorted(W.CHANNELIZERS))
+    ap.add_argument("--also", default=None,
+                    help="comma-separated further workloads measured in the same run and reported under "
+                         f"'also' (default: {','.join(DEFAULT_ALSO)} with the default workload, else none)")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="shorten a single-call workload to this many blocks (smaller profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--direct", action="store_true",
@@ -837,11 +886,19 @@ def main(argv=None):
         out = run_chan_reference(args, c, world, rank) if args.impl == "reference" else run_chan(
             args, c, world, rank, local)
     else:
-        w = W.WORKLOADS[args.config]
+        w = workload(args.config, args.blocks)
         if args.impl == "reference":
             out = run_reference(args, w, world, rank)
         else:
             out = run_ours(args, w, world, rank, local)
+            also = DEFAULT_ALSO if args.also is None and args.config == DEFAULT_CONFIG else \
+                [a for a in (args.also or "").split(",") if a]
+            if also:
+                out["also"] = []
+                for name in also:
+                    r = run_ours(args, workload(name, args.blocks), world, rank, local,
+                                 cpu_budget=min(args.cpu_budget, 6.0))
+                    out["also"].append({k: r[k] for k in ALSO_KEYS if k in r})
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     if world > 1 and args.impl == "ours":
