@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -42,6 +43,62 @@ int cuda_fail(cudaError_t e, const char *what) {
         cudaError_t e_ = (call);                      \
         if (e_ != cudaSuccess) return cuda_fail(e_, what); \
     } while (0)
+
+// Every allocation the library makes -- its plan objects and its device buffers -- goes
+// through alloc_take / dev_alloc and is returned through alloc_give / dev_free, which keep
+// the number of live allocations (fir_os_debug_live_allocs) and can be told to fail the k-th
+// next allocation as if memory had run out (fir_os_debug_fail_alloc): a host-side way to
+// reach every allocation-failure path without exhausting a device.
+std::atomic<long long> g_live_allocs{0};
+std::atomic<int> g_fail_countdown{0};
+
+// True when this allocation is the one chosen to fail.
+bool injected_failure() {
+    int k = g_fail_countdown.load();
+    while (k > 0 && !g_fail_countdown.compare_exchange_weak(k, k - 1)) {
+    }
+    return k == 1;
+}
+
+cudaError_t dev_alloc_raw(void **ptr, size_t bytes) {
+    *ptr = nullptr;
+    if (injected_failure()) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaMalloc(ptr, bytes);
+    if (e == cudaSuccess) ++g_live_allocs;
+    return e;
+}
+template <class T>
+cudaError_t dev_alloc(T **ptr, size_t bytes) {
+    void *v = nullptr;
+    const cudaError_t e = dev_alloc_raw(&v, bytes);
+    *ptr = static_cast<T *>(v);
+    return e;
+}
+void dev_free(void *ptr) {
+    if (!ptr) return;
+    cudaFree(ptr);
+    --g_live_allocs;
+}
+template <class T>
+T *alloc_take() {
+    if (injected_failure()) return nullptr;
+    T *p = new (std::nothrow) T;
+    if (p) ++g_live_allocs;
+    return p;
+}
+template <class T>
+void alloc_give(T *p) {
+    if (!p) return;
+    delete p;
+    --g_live_allocs;
+}
+
+// status of a failed device allocation: FIR_OS_E_NOMEM when memory ran out, else the CUDA error
+int alloc_fail(cudaError_t e, const char *what) {
+    cudaGetLastError();  // an allocation failure leaves no sticky error; clear the last-error slot
+    if (e == cudaErrorMemoryAllocation) return fail(FIR_OS_E_NOMEM, "%s: out of device memory", what);
+    return cuda_fail(e, what);
+}
 
 // ------------------------------------------------------------------ plan-time kernels
 
@@ -197,7 +254,9 @@ int noalloc_scratch(double2 **out) {
     if (!g_noalloc_ptr[dev]) {
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        // the first lookup on a device may load the library's device code there, which is when
+        // the array itself is allocated: running out of memory then is FIR_OS_E_NOMEM
+        if (e != cudaSuccess) return alloc_fail(e, "cudaGetSymbolAddress(static scratch)");
         g_noalloc_ptr[dev] = static_cast<double2 *>(ptr);
     }
     *out = g_noalloc_ptr[dev];
@@ -225,6 +284,7 @@ struct fir_os_plan {
     float2 *d_tw = nullptr;
     float2 *d_twa = nullptr;
     int *d_err = nullptr;
+    uint64_t wait_ns = fos::kWaitLimitNs;  // limit of a kernel's wait for one bulk copy
     // host-buffer path (lazily created)
     int64_t host_chunk = 0;
     void *hx[2] = {nullptr, nullptr};
@@ -256,26 +316,37 @@ struct DeviceScope {
     }
 };
 
-void free_plan(fir_os_plan *p) {
-    if (!p) return;
-    cudaFree(p->d_H);
-    cudaFree(p->d_Hk);
-    cudaFree(p->d_tw);
-    cudaFree(p->d_twa);
-    cudaFree(p->d_err);
+// The host-buffer path's device buffers, events and streams (created on its first call).
+void release_host_path(fir_os_plan *p) {
     for (int k = 0; k < 2; ++k) {
-        cudaFree(p->hx[k]);
-        cudaFree(p->hy[k]);
+        dev_free(p->hx[k]);
+        dev_free(p->hy[k]);
+        p->hx[k] = p->hy[k] = nullptr;
         if (p->ev_in[k]) cudaEventDestroy(p->ev_in[k]);
         if (p->ev_comp[k]) cudaEventDestroy(p->ev_comp[k]);
         if (p->ev_out[k]) cudaEventDestroy(p->ev_out[k]);
+        p->ev_in[k] = p->ev_comp[k] = p->ev_out[k] = nullptr;
     }
-    cudaFree(p->hstate);
+    dev_free(p->hstate);
+    p->hstate = nullptr;
     if (p->ev_start) cudaEventDestroy(p->ev_start);
     if (p->s_in) cudaStreamDestroy(p->s_in);
     if (p->s_comp) cudaStreamDestroy(p->s_comp);
     if (p->s_out) cudaStreamDestroy(p->s_out);
-    delete p;
+    p->ev_start = nullptr;
+    p->s_in = p->s_comp = p->s_out = nullptr;
+    p->host_chunk = 0;
+}
+
+void free_plan(fir_os_plan *p) {
+    if (!p) return;
+    dev_free(p->d_H);
+    dev_free(p->d_Hk);
+    dev_free(p->d_tw);
+    dev_free(p->d_twa);
+    dev_free(p->d_err);
+    release_host_path(p);
+    alloc_give(p);
 }
 
 // Stockham pass twiddles of a 2^logn-point per-CTA transform (layout in fos_fft.cuh),
@@ -346,6 +417,7 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.tw = p->d_tw;
     bp.twa = p->d_twa;
     bp.err = p->d_err;
+    bp.wait_ns = p->wait_ns;
     bp.n = n;
     bp.upc = units_for(p, n);
     bp.nunits = bp.upc * channels;
@@ -546,7 +618,7 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
         return fail(FIR_OS_E_ALIGN, "h must be naturally aligned");
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    fir_os_plan *p = new (std::nothrow) fir_os_plan;
+    fir_os_plan *p = alloc_take<fir_os_plan>();
     if (!p) return fail(FIR_OS_E_NOMEM, "plan allocation failed");
     int rc = FIR_OS_OK;
     auto bail = [&](int status) {
@@ -624,14 +696,13 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
     // device memory
     {
         cudaError_t e;
-        if ((e = cudaMalloc(&p->d_H, sizeof(float2) * N)) != cudaSuccess ||
-            (e = cudaMalloc(&p->d_err, sizeof(int))) != cudaSuccess)
-            return bail(e == cudaErrorMemoryAllocation ? fail(FIR_OS_E_NOMEM, "cudaMalloc failed")
-                                                       : cuda_fail(e, "cudaMalloc"));
+        if ((e = dev_alloc(&p->d_H, sizeof(float2) * N)) != cudaSuccess ||
+            (e = dev_alloc(&p->d_err, sizeof(int))) != cudaSuccess)
+            return bail(alloc_fail(e, "cudaMalloc(H, error word)"));
         std::vector<float2> tw;
         if (!pass_twiddles(p->kernel.fft_logn, tw)) return bail(fail(FIR_OS_E_UNSUPPORTED, "twiddles"));
-        if ((e = cudaMalloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess)
-            return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(twiddles) failed"));
+        if ((e = dev_alloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess)
+            return bail(alloc_fail(e, "cudaMalloc(twiddles)"));
         if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice,
                                  stream)) != cudaSuccess)
             return bail(cuda_fail(e, "twiddle upload"));
@@ -648,8 +719,8 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
                 const double ang = -2.0 * M_PI * (double)k / (double)HI;
                 twa[(size_t)C * 128 + k] = make_float2((float)std::cos(ang), (float)std::sin(ang));
             }
-            if ((e = cudaMalloc(&p->d_twa, sizeof(float2) * twa.size())) != cudaSuccess)
-                return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(split twiddles) failed"));
+            if ((e = dev_alloc(&p->d_twa, sizeof(float2) * twa.size())) != cudaSuccess)
+                return bail(alloc_fail(e, "cudaMalloc(split twiddles)"));
             if ((e = cudaMemcpyAsync(p->d_twa, twa.data(), sizeof(float2) * twa.size(), cudaMemcpyHostToDevice,
                                      stream)) != cudaSuccess)
                 return bail(cuda_fail(e, "split twiddle upload"));
@@ -665,10 +736,10 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
     if (coef_kind == FIR_OS_COEF_TIME) {
         double2 *A = nullptr, *B = nullptr;
         cudaError_t e;
-        if ((e = cudaMalloc(&A, sizeof(double2) * N)) != cudaSuccess ||
-            (e = cudaMalloc(&B, sizeof(double2) * N)) != cudaSuccess) {
-            cudaFree(A);
-            return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(plan scratch) failed"));
+        if ((e = dev_alloc(&A, sizeof(double2) * N)) != cudaSuccess ||
+            (e = dev_alloc(&B, sizeof(double2) * N)) != cudaSuccess) {
+            dev_free(A);
+            return bail(alloc_fail(e, "cudaMalloc(plan scratch)"));
         }
         fos_fill_h64<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, coef_dev, M, N, coef_complex);
         for (int Ns = 1; Ns < N; Ns *= 2) {
@@ -680,8 +751,8 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
         fos_finish_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(A, p->d_H, N);
         e = cudaGetLastError();
         cudaError_t e2 = cudaStreamSynchronize(stream);
-        cudaFree(A);
-        cudaFree(B);
+        dev_free(A);
+        dev_free(B);
         if (e != cudaSuccess) return bail(cuda_fail(e, "frequency-response kernels"));
         if (e2 != cudaSuccess) return bail(cuda_fail(e2, "frequency-response sync"));
     } else {
@@ -708,8 +779,8 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
     }
     if (p->kernel.split_c > 0) {
         // the resident kernel reads H[c + C d] for one c at a time: store it c-major
-        cudaError_t e = cudaMalloc(&p->d_Hk, sizeof(float2) * N);
-        if (e != cudaSuccess) return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc(H, c-major) failed"));
+        cudaError_t e = dev_alloc(&p->d_Hk, sizeof(float2) * N);
+        if (e != cudaSuccess) return bail(alloc_fail(e, "cudaMalloc(H, c-major)"));
         fos_permute_h<<<(N + tpb - 1) / tpb, tpb, 0, stream>>>(p->d_H, p->d_Hk, N, p->kernel.split_c);
         if ((e = cudaGetLastError()) != cudaSuccess) return bail(cuda_fail(e, "H permute kernel"));
         if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return bail(cuda_fail(e, "H permute sync"));
@@ -726,6 +797,22 @@ int fir_os_plan_destroy(fir_os_plan_t plan) {
     free_plan(plan);
     return FIR_OS_OK;
 }
+
+int fir_os_plan_set_wait_limit(fir_os_plan_t plan, int64_t limit_ns) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (limit_ns < 0 || limit_ns > 60LL * 1000000000LL)
+        return fail(FIR_OS_E_INVAL, "wait limit %lld ns is outside [0, 60 s]", (long long)limit_ns);
+    plan->wait_ns = (uint64_t)limit_ns;
+    return FIR_OS_OK;
+}
+
+int fir_os_debug_fail_alloc(int k) {
+    if (k < 0) return fail(FIR_OS_E_INVAL, "k = %d < 0", k);
+    g_fail_countdown.store(k);
+    return FIR_OS_OK;
+}
+
+int64_t fir_os_debug_live_allocs(void) { return (int64_t)g_live_allocs.load(); }
 
 int fir_os_plan_info(fir_os_plan_t plan, int *M, int *N, int *L) {
     if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
@@ -855,20 +942,30 @@ int fir_os_execute_host(fir_os_plan_t plan, const void *x_host, int64_t n, void 
         int64_t chunk = ((int64_t)1 << 21) / span * span;
         if (chunk < span) chunk = span;
         plan->host_chunk = chunk;
-        for (int k = 0; k < 2; ++k) {
-            cudaError_t e1 = cudaMalloc(&plan->hx[k], (size_t)chunk * sb);
-            cudaError_t e2 = cudaMalloc(&plan->hy[k], (size_t)chunk * sb);
-            if (e1 != cudaSuccess || e2 != cudaSuccess) return fail(FIR_OS_E_NOMEM, "cudaMalloc(host path buffers)");
-            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_in[k], cudaEventDisableTiming), "event");
-            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_comp[k], cudaEventDisableTiming), "event");
-            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_out[k], cudaEventDisableTiming), "event");
+        // on any failure everything made so far is released, so a later call starts afresh
+        const int st = [&]() -> int {
+            cudaError_t e;
+            for (int k = 0; k < 2; ++k) {
+                if ((e = dev_alloc(&plan->hx[k], (size_t)chunk * sb)) != cudaSuccess ||
+                    (e = dev_alloc(&plan->hy[k], (size_t)chunk * sb)) != cudaSuccess)
+                    return alloc_fail(e, "cudaMalloc(host path buffers)");
+                FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_in[k], cudaEventDisableTiming), "event");
+                FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_comp[k], cudaEventDisableTiming), "event");
+                FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_out[k], cudaEventDisableTiming), "event");
+            }
+            if (plan->M > 1 && (e = dev_alloc(&plan->hstate, sbytes)) != cudaSuccess)
+                return alloc_fail(e, "cudaMalloc(host path state)");
+            FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_start, cudaEventDisableTiming), "event");
+            FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking), "stream");
+            FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking), "stream");
+            FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_comp, cudaStreamNonBlocking), "stream");
+            return FIR_OS_OK;
+        }();
+        if (st != FIR_OS_OK) {
+            release_host_path(plan);
+            return st;
         }
-        if (plan->M > 1 && cudaMalloc(&plan->hstate, sbytes) != cudaSuccess)
-            return fail(FIR_OS_E_NOMEM, "cudaMalloc(host path state)");
-        FOS_CUDA(cudaEventCreateWithFlags(&plan->ev_start, cudaEventDisableTiming), "event");
-        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking), "stream");
-        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking), "stream");
-        FOS_CUDA(cudaStreamCreateWithFlags(&plan->s_comp, cudaStreamNonBlocking), "stream");
+        plan->host_chunk = chunk;
     }
     const int64_t chunk = plan->host_chunk;
     FOS_CUDA(cudaEventRecord(plan->ev_start, caller), "event record");
@@ -968,9 +1065,9 @@ int fir_chan_plan_destroy(fir_chan_plan_t plan) {
     if (!plan) return FIR_OS_OK;
     DeviceScope on(plan->device);
     cudaDeviceSynchronize();
-    cudaFree(plan->d_h);
-    cudaFree(plan->d_tw);
-    delete plan;
+    dev_free(plan->d_h);
+    dev_free(plan->d_tw);
+    alloc_give(plan);
     return FIR_OS_OK;
 }
 
@@ -1003,7 +1100,7 @@ int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_ki
         return fail(FIR_OS_E_UNSUPPORTED, "a prototype of %d taps (%d per branch) does not fit shared memory "
                                           "with K = %d (at most %d taps)",
                     Nh, P, K, (int)((prop.sharedMemPerBlockOptin - k.smem_fixed) / (4 * K)) * K);
-    fir_chan_plan *p = new (std::nothrow) fir_chan_plan;
+    fir_chan_plan *p = alloc_take<fir_chan_plan>();
     if (!p) return fail(FIR_OS_E_NOMEM, "plan allocation failed");
     auto bail = [&](int status) {
         fir_chan_plan_destroy(p);
@@ -1027,9 +1124,9 @@ int fir_chan_plan_create(fir_chan_plan_t *out, int K, int D, int Nh, int data_ki
     p->max_ctas = per_sm * prop.multiProcessorCount;
     std::vector<float2> tw;
     if (!pass_twiddles(logk, tw)) return bail(fail(FIR_OS_E_UNSUPPORTED, "twiddles"));
-    if ((e = cudaMalloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess ||
-        (e = cudaMalloc(&p->d_h, sizeof(float) * (size_t)P * K)) != cudaSuccess)
-        return bail(fail(FIR_OS_E_NOMEM, "cudaMalloc failed"));
+    if ((e = dev_alloc(&p->d_tw, sizeof(float2) * tw.size())) != cudaSuccess ||
+        (e = dev_alloc(&p->d_h, sizeof(float) * (size_t)P * K)) != cudaSuccess)
+        return bail(alloc_fail(e, "cudaMalloc(channelizer tables)"));
     // the prototype zero-padded to P K taps, so that the kernel reads it in whole 16-byte pieces
     if ((e = cudaMemcpyAsync(p->d_tw, tw.data(), sizeof(float2) * tw.size(), cudaMemcpyHostToDevice, stream)) !=
             cudaSuccess ||

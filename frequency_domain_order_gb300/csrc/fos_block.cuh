@@ -7,7 +7,9 @@
 //            groups of blocks arrive by one bulk (TMA) copy issued while the previous group
 //            is being transformed (double-buffered); for groups that touch the state S0 or run
 //            past the input, the part inside x comes by bulk copy and the rest (S0 in front,
-//            the ragged ends, zeros behind) by plain loads.
+//            the ragged ends, zeros behind) by plain loads.  The wait for a copy is bounded
+//            (BlockParams::wait_ns); a copy that misses it sets the error word, the group waits
+//            (bounded again) for that copy to land and then gathers with plain loads only.
 //   FFT      F_i = FFT_N(E_i) in registers and two alternating exchange buffers
 //   multiply I_i = F_i * H
 //   IFFT     R_i = IFFT_N(I_i), natural order in registers
@@ -372,15 +374,21 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
             onxt = stage_unit<LOGN, REAL>(p, chan<REAL>(p, chn), lun, nxt, bnxt, allow_tma, unxt, tg, gbar);
         }
         if (ucur) {
-            const bool ok = mbar_wait_bounded(bcur, pcur);
-            pcur ^= 1u;
+            const bool ok = mbar_wait_bounded(bcur, pcur, p.wait_ns);
             if (gbar.sync_or(!ok)) {
-                // the copy did not arrive in time: report it, stop using bulk copies and
-                // gather this unit with plain loads instead
+                // the copy did not arrive within the limit: report it and stop issuing bulk
+                // copies.  The copy still targets `cur` and completes on its mbarrier, so before
+                // `cur` is written again the group waits (bounded by the fixed second limit)
+                // for that phase; then it gathers this unit with plain loads.  A copy that
+                // misses the second limit too leaves `cur` unusable: the group stops (its
+                // remaining units are not filtered) with the error word set.
                 if (tg == 0) atomicExch(p.err, 1);
                 allow_tma = false;
+                const bool landed = mbar_wait_bounded(bcur, pcur, kWaitLimitNs);
+                if (gbar.sync_or(!landed)) break;
                 ocur = stage_unit<LOGN, REAL>(p, chan<REAL>(p, chu), lu, cur, bcur, false, ucur, tg, gbar);
             }
+            pcur ^= 1u;  // that phase has completed
         }
 
         // gather E_i (step 3) from the staged window into registers: v[e] = E[j + e T]

@@ -210,16 +210,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Longest a kernel waits for one bulk copy before it reports FIR_OS_E_DEVICE (1 s).
+// Default limit of a kernel's wait for one bulk copy before it reports FIR_OS_E_DEVICE (1 s; a
+// plan may set another, fir_os_plan_set_wait_limit), and the fixed limit of the second wait
+// that lets a copy which missed the first one land before its buffer is reused.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Bounded wait for the phase with the given parity to complete; false if it ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete; false if it ran out.  A limit
+// of 0 runs out before the first poll (every such wait fails: the setting that tests the
+// fallback).  The poll count is bounded too, in case the timer stops.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns == 0) return false;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

@@ -17,6 +17,7 @@ struct BlockParams {
     const float2 *twa;     // resident / pair kernels: W_N^{r c} at [c * 128 + r] (c < C),
                            // then W_N^{128 k} at [C * 128 + k] (k < N / 128)
     int *err;              // device error word (set to 1 when a bounded wait ran out)
+    uint64_t wait_ns;      // limit of one bounded wait for a bulk copy (0: every wait runs out)
     int64_t n;             // samples in this call (per channel)
     int64_t nunits;        // work units of all channels (block groups / blocks / block pairs)
     int64_t upc;           // work units per channel; unit u is unit u mod upc of channel u / upc

@@ -41,6 +41,9 @@ SIGNATURES = {
     "fir_os_plan_kernel": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                                 ctypes.POINTER(_I)]),
     "fir_os_device_status": (_I, [_P, _P]),
+    "fir_os_plan_set_wait_limit": (_I, [_P, _I64]),
+    "fir_os_debug_fail_alloc": (_I, [_I]),
+    "fir_os_debug_live_allocs": (_I64, []),
     "fir_os_launches": (_I, [_P, _I64]),
     "fir_os_frequency_response_noalloc": (_I, [_P, _I, _I, _I, _P, _P]),
     "fir_os_choose_n": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
@@ -77,6 +80,16 @@ def fp32_probe(iters: int, stream=None) -> float:
     f = ctypes.c_double()
     _check(lib().fir_os_fp32_probe(int(iters), _stream_handle(stream), ctypes.byref(f)))
     return f.value
+
+
+def debug_fail_alloc(k: int):
+    """fir_os_debug_fail_alloc: the k-th next allocation of the library fails (0 disarms)."""
+    _check(lib().fir_os_debug_fail_alloc(int(k)))
+
+
+def debug_live_allocs() -> int:
+    """fir_os_debug_live_allocs: the library's live allocations (plan objects, device buffers)."""
+    return int(lib().fir_os_debug_live_allocs())
 
 
 class FirOsError(RuntimeError):
@@ -204,6 +217,11 @@ class Plan:
 
     def device_status(self, stream=None):
         _check(lib().fir_os_device_status(self._h, _stream_handle(stream)))
+
+    def set_wait_limit(self, limit_ns: int):
+        """fir_os_plan_set_wait_limit: the kernels' limit for one bulk-copy wait (0: every wait
+        runs out at once and the fallback gather runs)."""
+        _check(lib().fir_os_plan_set_wait_limit(self._h, int(limit_ns)))
 
     def close(self):
         if getattr(self, "_h", None):

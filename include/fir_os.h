@@ -184,6 +184,29 @@ int fir_os_launches(fir_os_plan_t plan, int64_t n_samples);
  * last check. */
 int fir_os_device_status(fir_os_plan_t plan, void *stream);
 
+/* fir_os_plan_set_wait_limit -- the longest a kernel of this plan waits for one bulk copy of
+ * its input window (step 3 of the claim, the overlap gather, which the N <= 8192 kernels stage
+ * into shared memory by bulk copies) before it gives up on that copy: 1 s by default.  A wait
+ * that runs out sets the plan's error word (fir_os_device_status then returns FIR_OS_E_DEVICE);
+ * the kernel lets that copy land (a second wait of at most 1 s) and gathers the window, and
+ * every later one of the same launch, with plain loads instead, so the outputs are still
+ * correct.  limit_ns = 0 makes every such wait run out at once -- a way to run the fallback
+ * on a healthy device; the N >= 16384 kernels have no such waits.  Applies to launches
+ * enqueued after the call.  FIR_OS_E_INVAL for a NULL plan or a limit outside [0, 60 s]. */
+int fir_os_plan_set_wait_limit(fir_os_plan_t plan, int64_t limit_ns);
+
+/* fir_os_debug_fail_alloc -- make the k-th next allocation of the library (its plan objects
+ * and the device buffers of fir_os_plan_create, fir_chan_plan_create and the first
+ * fir_os_execute_host call) fail as if memory had run out, without asking CUDA; k = 0
+ * disarms.  The failing call returns FIR_OS_E_NOMEM and releases everything it had allocated.
+ * A process-wide host-side test hook (not for concurrent use); FIR_OS_E_INVAL for k < 0. */
+int fir_os_debug_fail_alloc(int k);
+
+/* fir_os_debug_live_allocs -- the number of the library's allocations (plan objects and device
+ * buffers) alive now, process-wide; with fir_os_debug_fail_alloc it shows that a failed call
+ * left nothing behind. */
+int64_t fir_os_debug_live_allocs(void);
+
 /*
  * fir_os_frequency_response_noalloc -- H = FFT_N(h zero-padded to N), the unscaled
  * complex64 response that fir_os_plan_create accepts as FIR_OS_COEF_FREQ, computed on the
@@ -193,7 +216,11 @@ int fir_os_device_status(fir_os_plan_t plan, void *stream);
  * real-time threads that cannot afford an allocation's unbounded latency, or a process that
  * is at its memory limit.  fir_os_plan_create needs float64 working buffers for the same
  * transform and allocates them; this call uses a fixed 2 MiB array in the library's device
- * image instead (held by every device that loads the library until the process exits).
+ * image instead.  CUDA allocates that array on a device when the library's device code is
+ * loaded there (with lazy module loading, the default: at the library's first kernel launch or
+ * symbol lookup on that device, which may be this call's), and holds it until the process
+ * exits; so make one call (or create a plan) early, outside stream capture and away from the
+ * device's memory limit.  If loading runs out of memory the call returns FIR_OS_E_NOMEM.
  *
  *   h_dev      M taps (device): float32 if h_complex == 0, complex64 if 1, naturally aligned
  *   M          1 <= M <= N

@@ -84,3 +84,25 @@ def test_no_device_is_an_error_not_a_crash(L):
         pytest.skip("a GPU is present")
     rc, h = _create(L, 64, 256)
     assert rc == fir_os.E_CUDA and not h.value
+
+
+def test_test_hooks_reject_bad_arguments(L):
+    assert L.fir_os_plan_set_wait_limit(None, 0) == fir_os.E_INVAL
+    assert L.fir_os_debug_fail_alloc(-1) == fir_os.E_INVAL
+    assert L.fir_os_debug_fail_alloc(0) == fir_os.OK
+
+
+def test_injected_allocation_failure_is_nomem_and_leaks_nothing(L):
+    """The first allocation of fir_os_plan_create is its host-side plan object, made before any
+    device call: an injected failure there returns FIR_OS_E_NOMEM, no plan, and leaves the
+    library's live-allocation count unchanged (GPU tests cover the device buffers)."""
+    before = L.fir_os_debug_live_allocs()
+    assert L.fir_os_debug_fail_alloc(1) == fir_os.OK
+    rc, h = _create(L, 64, 256)
+    assert rc == fir_os.E_NOMEM and not h.value
+    assert b"plan allocation" in L.fir_os_last_error()
+    assert L.fir_os_debug_live_allocs() == before
+    # the hook fired once and is spent: the next call gets past the plan object
+    rc, h = _create(L, 8, 64, data_kind=7)
+    assert rc == fir_os.E_INVAL
+    assert L.fir_os_debug_fail_alloc(0) == fir_os.OK

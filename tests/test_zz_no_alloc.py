@@ -4,9 +4,10 @@ fir_os_frequency_response_noalloc exists for callers that may not allocate devic
 they build a filter's response (their device memory belongs to their own pool, they run on a
 real-time thread, or the device is at its memory limit).  It computes the same float64 step-1
 transform that fir_os_plan_create runs with allocated buffers, but in a fixed array inside the
-library.  This file checks, on two calls in a row, that filtering with its response matches
-filtering with the plan that computes the response itself, under the same parity bar as the
-other GPU tests.  It sits last in collection order so that a stop-at-first-failure run has
+library.  This file checks, on consecutive calls, that its response matches numpy's float64 FFT
+of the taps, and that filtering with it matches both the float64 oracle (direct convolution)
+and filtering with the plan that computes the response itself, under the same parity bar as
+the other GPU tests.  It sits last in collection order so that a stop-at-first-failure run has
 already run everything else.
 """
 import ctypes
@@ -73,6 +74,10 @@ def test_consecutive_calls_match_the_allocating_path(fo):
         rel_tol, abs_tol = W.tolerance(W.oracle_h(w), x)
         rel, mx = W.errors(y_given, y_alloc)
         assert rel <= rel_tol and mx <= abs_tol, (w.name, rel, mx)
+        import oracle
+        want, _ = oracle.direct(x, W.oracle_h(w))
+        rel, mx = W.errors(y_given, want)
+        assert rel <= rel_tol and mx <= abs_tol, (w.name, "against the oracle", rel, mx)
         outs.append(y_given)
     assert len(outs) == 3
 
