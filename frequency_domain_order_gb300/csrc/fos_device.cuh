@@ -21,12 +21,14 @@ namespace fos {
 // --------------------------------------------------------------------------- complex ops
 
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
-// one packed f32x2 instruction per complex add / subtract
+// one packed f32x2 instruction per complex add / subtract / component-wise multiply-add
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 csub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+__device__ __forceinline__ float2 cfma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 #else
 FOS_HD float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 FOS_HD float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+FOS_HD float2 cfma2(float2 a, float2 b, float2 c) { return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y)); }
 #endif
 FOS_HD float2 cneg(float2 a) { return make_float2(-a.x, -a.y); }
 
@@ -120,30 +122,48 @@ FOS_HD void dft2(float2 &a0, float2 &a1) {
     a1 = csub(t, a1);
 }
 
-template <int DIR>
+// PQ selects how the quarter turn of t3 = a1 - a3 is formed: false as scalar adds on t3's
+// components; true with t3 formed component-swapped, so that a1, a3 = t1 +- (DIR i) t3 are one
+// packed multiply-add each.  Both give identical results; which issues faster depends on the
+// kernel around it (measured per kernel).
+template <int DIR, bool PQ = false>
 FOS_HD void dft4(float2 &a0, float2 &a1, float2 &a2, float2 &a3) {
-    const float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), t3 = csub(a1, a3);
-    a0 = cadd(t0, t2);
-    a2 = csub(t0, t2);
-    // t1 +- (DIR i) t3, component by component (a quarter turn swaps re and im)
-    if constexpr (DIR < 0) {
-        a1 = make_float2(t1.x + t3.y, t1.y - t3.x);
-        a3 = make_float2(t1.x - t3.y, t1.y + t3.x);
+    const float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3);
+    if constexpr (PQ) {
+        const float2 s = make_float2(a1.y - a3.y, a1.x - a3.x);  // (t3.y, t3.x)
+        a0 = cadd(t0, t2);
+        a2 = csub(t0, t2);
+        if constexpr (DIR < 0) {  // t1 - i t3 = (t1.x + t3.y, t1.y - t3.x)
+            a1 = cfma2(s, make_float2(1.f, -1.f), t1);
+            a3 = cfma2(s, make_float2(-1.f, 1.f), t1);
+        } else {
+            a1 = cfma2(s, make_float2(-1.f, 1.f), t1);
+            a3 = cfma2(s, make_float2(1.f, -1.f), t1);
+        }
     } else {
-        a1 = make_float2(t1.x - t3.y, t1.y + t3.x);
-        a3 = make_float2(t1.x + t3.y, t1.y - t3.x);
+        const float2 t3 = csub(a1, a3);
+        a0 = cadd(t0, t2);
+        a2 = csub(t0, t2);
+        // t1 +- (DIR i) t3, component by component (a quarter turn swaps re and im)
+        if constexpr (DIR < 0) {
+            a1 = make_float2(t1.x + t3.y, t1.y - t3.x);
+            a3 = make_float2(t1.x - t3.y, t1.y + t3.x);
+        } else {
+            a1 = make_float2(t1.x - t3.y, t1.y + t3.x);
+            a3 = make_float2(t1.x + t3.y, t1.y - t3.x);
+        }
     }
 }
 
 // R = R1 * 4 with n = 4 a + b, k = c + R1 d:
 //   X[c + R1 d] = sum_b W4^{bd} W_R^{bc} sum_a x[4a + b] W_R1^{ac}
-template <int R, int DIR>
+template <int R, int DIR, bool PQ = false>
 FOS_HD void dft(float2 *a) {
     if constexpr (R == 1) {
     } else if constexpr (R == 2) {
         dft2<DIR>(a[0], a[1]);
     } else if constexpr (R == 4) {
-        dft4<DIR>(a[0], a[1], a[2], a[3]);
+        dft4<DIR, PQ>(a[0], a[1], a[2], a[3]);
     } else {
         constexpr int R1 = R / 4;
         float2 y[4][R1];
@@ -151,7 +171,7 @@ FOS_HD void dft(float2 *a) {
         for (int b = 0; b < 4; ++b) {
 #pragma unroll
             for (int q = 0; q < R1; ++q) y[b][q] = a[4 * q + b];
-            dft<R1, DIR>(y[b]);
+            dft<R1, DIR, PQ>(y[b]);
         }
         // twiddles W_R^{bc}
 #pragma unroll
@@ -162,7 +182,7 @@ FOS_HD void dft(float2 *a) {
         }
 #pragma unroll
         for (int c = 0; c < R1; ++c) {
-            dft4<DIR>(y[0][c], y[1][c], y[2][c], y[3][c]);
+            dft4<DIR, PQ>(y[0][c], y[1][c], y[2][c], y[3][c]);
 #pragma unroll
             for (int d = 0; d < 4; ++d) a[c + R1 * d] = y[d][c];
         }

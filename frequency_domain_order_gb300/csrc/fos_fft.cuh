@@ -71,7 +71,7 @@ struct TwLayout {
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
 // transform's last pass reads.  Every buffer is xpad_len(N) elements of this transform.
 
-template <int LOGN, int SMAX, int P, bool INV, class Bar>
+template <int LOGN, int SMAX, int P, bool INV, bool PQ, class Bar>
 __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
                                             uint32_t tm, int j, const Bar &bar) {
     using S = FftShape<LOGN>;
@@ -108,7 +108,7 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
 #pragma unroll
             for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
         }
-        dft<16, DIR>(v);
+        dft<16, DIR, PQ>(v);
         if constexpr (!last) {
             const int base = (j / Ns) * (16 * Ns) + m;
             if constexpr (Ns % 16 == 0) {
@@ -121,14 +121,14 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, SMAX, P + 1, INV>(v, b0, b1, stw, tm, j, bar);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ>(v, b0, b1, stw, tm, j, bar);
     }
 }
 
 // Transform v in place (layout z[j + e T] -> Z[j + e T]).  `bar` synchronises the threads that
 // share the two buffers.  No barrier is needed before the first write: see the buffer rotation
-// above and the callers' barrier placement.
-template <int LOGN, int SMAX, bool INV, class Bar>
+// above and the callers' barrier placement.  PQ: the quarter-turn form of dft4 (fos_device.cuh).
+template <int LOGN, int SMAX, bool INV, bool PQ = false, class Bar>
 __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
                                        int j, const Bar &bar) {
     using S = FftShape<LOGN>;
@@ -141,7 +141,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
         float2 a[R0];
 #pragma unroll
         for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
-        dft<R0, DIR>(a);
+        dft<R0, DIR, PQ>(a);
 #pragma unroll
         for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
     }
@@ -158,7 +158,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, SMAX, 1, INV>(v, b0, b1, stw, tm, j, bar);
+    fft_tm_pass<LOGN, SMAX, 1, INV, PQ>(v, b0, b1, stw, tm, j, bar);
 }
 
 }  // namespace fos

@@ -66,15 +66,37 @@ struct PairCfg {
 
 __device__ __forceinline__ int recv_index(int a, int m, int r) { return (a * 16 + (m & 15)) * 128 + r; }
 
-template <bool REAL>
-__device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, int s, int r, const float2 *hi_s,
-                                              const float2 *wr_s, uint32_t peer_recv) {
-    using Q = PairCfg<REAL>;
-    constexpr int HI = Q::HI;
-    const bool own = (uint32_t)(s >> 1) == kappa;
-    float2 wr[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) wr[c] = wr_s[(kappa + 2 * c) * 128 + r];
+// w[c'] = W_N^{b c} for this CTA's bins c = KAPPA + 2 c', c' < 8 (w[0] = 1 for KAPPA = 0 is not
+// written), from g = W_N^b by squarings and products: no power is more than four complex
+// multiplications from g.
+template <int KAPPA>
+__device__ __forceinline__ void pair_twiddles(float2 g, float2 (&w)[8]) {
+    const float2 h = cmul(g, g);  // W_N^{2b}
+    if constexpr (KAPPA == 0) {
+        w[1] = h;
+        w[2] = cmul(h, h);
+        w[3] = cmul(w[2], h);
+        w[4] = cmul(w[2], w[2]);
+        w[5] = cmul(w[4], h);
+        w[6] = cmul(w[4], w[2]);
+        w[7] = cmul(w[4], w[3]);
+    } else {
+        const float2 h2 = cmul(h, h), h4 = cmul(h2, h2);  // W_N^{4b}, W_N^{8b}
+        w[0] = g;
+        w[1] = cmul(g, h);
+        w[2] = cmul(g, h2);
+        w[3] = cmul(w[1], h2);
+        w[4] = cmul(g, h4);
+        w[5] = cmul(w[1], h4);
+        w[6] = cmul(w[2], h4);
+        w[7] = cmul(w[3], h4);
+    }
+}
+
+template <bool REAL, int KAPPA>
+__device__ __forceinline__ void pair_phase_c1(uint32_t tlane, int s, int r, const float2 *hi_s, float2 wr1,
+                                              uint32_t peer_recv) {
+    const bool own = (s >> 1) == KAPPA;
 #pragma unroll 1
     for (int st = 0; st < 4; ++st) {
         const int i0 = (st & 1) + 4 * (st >> 1);
@@ -86,11 +108,10 @@ __device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, in
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int m = 8 * s + i0 + 2 * h;
+            float2 w[8];  // W_N^b = W_N^r W_N^{128 m} (m < 32), then its powers
+            pair_twiddles<KAPPA>(cmul(wr1, hi_s[m]), w);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int cc = (int)kappa + 2 * c;
-                if (cc != 0) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * cc) & (HI - 1)]));
-            }
+            for (int c = KAPPA == 0 ? 1 : 0; c < 8; ++c) v[h][c] = cmulc(v[h][c], w[c]);
             dft<8, +1>(v[h]);
         }
         if (own) {
@@ -115,12 +136,12 @@ __device__ __forceinline__ void pair_phase_c1(uint32_t kappa, uint32_t tlane, in
 // slots (a', m) that it then overwrites with unit ua's values (c', m); the other range's slots
 // were freed by phase C1.  Each m starts with unit ua's 16 loads, so their latency overlaps the
 // combine and the stores.
-template <bool REAL>
+template <bool REAL, int KAPPA>
 __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc, void *yc, int64_t ua,
-                                               const Chan &cha, uint32_t kappa, uint32_t tlane, int s, int r,
-                                               const float2 *hi_s, const float2 *wr_s, const float2 *recv) {
+                                               const Chan &cha, uint32_t tlane, int s, int r,
+                                               const float2 *hi_s, float2 wr1, const float2 *recv) {
     using Q = PairCfg<REAL>;
-    constexpr int P = Q::P, HI = Q::HI;
+    constexpr int P = Q::P;
     // uc, ua: unit indices within their channels; yc: uc's channel's output, cha: ua's channel
     const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
     const bool whole = sc + Q::N + (REAL ? p.L : 0) <= p.n;
@@ -129,12 +150,9 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
     const int lim = p.n - sc > (int64_t)Q::N + p.L ? Q::N + p.L : (int)(p.n - sc);
     const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
     const bool interior = sa >= 0 && sa + Q::N + (REAL ? p.L : 0) <= p.n;
-    float2 wr[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) wr[c] = wr_s[(kappa + 2 * c) * 128 + r];
 #pragma unroll 1
     for (int q = 0; q < 8; ++q) {
-        const int rho = (q < 4) ? (int)kappa : 1 - (int)kappa;
+        const int rho = (q < 4) ? KAPPA : 1 - KAPPA;
         const int m = 16 * rho + 4 * s + (q & 3);
         const int b = r + 128 * m;
         const uint32_t col = 2u * (uint32_t)(16 * (m & 1) + (m >> 1));  // slot (0, m); + 64 per a' or c'
@@ -148,8 +166,8 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
                 const float2 other = recv[recv_index(a, m, r)];
-                const float2 p0 = kappa == 0 ? pown[a] : other;
-                const float2 p1 = kappa == 0 ? other : pown[a];
+                const float2 p0 = KAPPA == 0 ? pown[a] : other;
+                const float2 p1 = KAPPA == 0 ? other : pown[a];
                 const float2 w = ctw_dyn<16, +1>(p1, a);  // W_16^{-a'} P_1
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -170,7 +188,7 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
         }
         if (ua >= 0) {
             float2 v[8];
-            if (kappa == 0) {
+            if constexpr (KAPPA == 0) {
 #pragma unroll
                 for (int a = 0; a < 8; ++a) v[a] = cadd(x[a], x[a + 8]);
             } else {
@@ -178,16 +196,58 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
                 for (int a = 0; a < 8; ++a) v[a] = ctw_dyn<16, -1>(csub(x[a], x[a + 8]), a);
             }
             dft<8, -1>(v);
+            float2 w[8];
+            pair_twiddles<KAPPA>(cmul(wr1, hi_s[m]), w);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int cc = (int)kappa + 2 * c;
-                if (cc != 0) v[c] = cmul(v[c], cmul(wr[c], hi_s[(m * cc) & (HI - 1)]));
-            }
+            for (int c = KAPPA == 0 ? 1 : 0; c < 8; ++c) v[c] = cmul(v[c], w[c]);
 #pragma unroll
             for (int c = 0; c < 8; ++c) tmem_st2(tlane + 64u * c + col, v[c]);
         }
     }
     if (ua >= 0) tmem_wait_st();
+}
+
+// The block loop of CTA KAPPA of a cluster (a copy per rank, so that every rank-dependent choice
+// is made at compile time).
+template <bool REAL, bool MULTI, int KAPPA>
+__device__ __forceinline__ void pair_loop(const BlockParams &p, int64_t u, int64_t uend, int tid, int warp, int s,
+                                          int r, int g, int j, uint32_t tlane, const float2 *stw,
+                                          const float2 *hi_s, float2 wr1, float2 *bufs, float2 *b0, float2 *b1,
+                                          uint32_t peer_recv, const GroupBarrier<256> &gbar) {
+    using Q = PairCfg<REAL>;
+    int64_t lu = 0, lun = 0;
+    int chu = u < uend ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
+    if (u < uend)  // phase A of the first unit
+        pair_phase_c2a<REAL, KAPPA>(p, -1, nullptr, lu, chan<REAL>(p, chu), tlane, s, r, hi_s, wr1, bufs);
+    for (; u < uend; ++u) {
+        tmem_fence_before_sync();
+        __syncthreads();
+        tmem_fence_after_sync();
+        const int64_t un = u + 1;
+        const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
+        if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, KAPPA, 2);
+        phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, KAPPA, 2, 32u * (uint32_t)((warp >> 2) & 1));
+        tmem_fence_before_sync();
+        cluster_sync();  // both CTAs are past phase B (and past every read of S0)
+        tmem_fence_after_sync();
+        if (KAPPA == 0 && p.fuse_state && lu == 0) {
+            // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
+            // last M-1 samples of the channel's x
+            using T_ = typename std::conditional<REAL, float, float2>::type;
+            const Chan cu = chan<REAL>(p, chu);
+            const T_ *x = static_cast<const T_ *>(cu.x);
+            T_ *st = static_cast<T_ *>(cu.state);
+            for (int t = tid; t < p.M - 1; t += Q::THREADS) st[t] = x[p.n - (p.M - 1) + t];
+        }
+        pair_phase_c1<REAL, KAPPA>(tlane, s, r, hi_s, wr1, peer_recv);
+        tmem_fence_before_sync();
+        cluster_sync();  // the other CTA's P values have landed in bufs
+        tmem_fence_after_sync();
+        pair_phase_c2a<REAL, KAPPA>(p, lu, chan<REAL>(p, chu).y, un < uend ? lun : -1, chan<REAL>(p, chn), tlane, s,
+                                    r, hi_s, wr1, bufs);
+        chu = chn;
+        lu = lun;
+    }
 }
 
 template <bool REAL, bool MULTI>
@@ -215,10 +275,13 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     // a contiguous range of units per cluster (at most one cluster per unit); both CTAs of a
     // cluster take the same units
     const int64_t ncl = nclusters_x();
-    int64_t u = (int64_t)cluster_id_x() * p.nunits / ncl, lu = 0, lun = 0;
+    const int64_t u = (int64_t)cluster_id_x() * p.nunits / ncl;
     const int64_t uend = ((int64_t)cluster_id_x() + 1) * p.nunits / ncl;
-    int chu = u < uend ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
-    if (u < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chu), lu, tid, (int)kappa, 2);  // a hint
+    if (u < uend && !p.no_bulk) {  // a hint
+        int64_t lu = 0;
+        const int chu = channel_of<MULTI>(p, u, lu);
+        prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chu), lu, tid, (int)kappa, 2);
+    }
     if (warp == 0) {
         tmem_alloc(tm_slot, Q::TM_COLS);
         tmem_relinquish();
@@ -230,40 +293,16 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     cluster_sync();  // both CTAs are running (and set up) before any remote store
     tmem_fence_after_sync();
     const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float2 wr1 = wr_s[128 + r];  // W_N^r
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
-    if (u < uend)  // phase A of the first unit
-        pair_phase_c2a<REAL>(p, -1, nullptr, lu, chan<REAL>(p, chu), kappa, tlane, s, r, hi_s, wr_s, bufs);
-    for (; u < uend; ++u) {
-        tmem_fence_before_sync();
-        __syncthreads();
-        tmem_fence_after_sync();
-        const int64_t un = u + 1;
-        const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
-        if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, (int)kappa, 2);
-        phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, (int)kappa, 2, 32u * (uint32_t)((warp >> 2) & 1));
-        tmem_fence_before_sync();
-        cluster_sync();  // both CTAs are past phase B (and past every read of S0)
-        tmem_fence_after_sync();
-        if (p.fuse_state && lu == 0 && kappa == 0) {
-            // only the channel's unit 0 reads its S0 (fuse_state), and n >= M - 1: S0' = the
-            // last M-1 samples of the channel's x
-            using T_ = typename std::conditional<REAL, float, float2>::type;
-            const Chan cu = chan<REAL>(p, chu);
-            const T_ *x = static_cast<const T_ *>(cu.x);
-            T_ *st = static_cast<T_ *>(cu.state);
-            for (int t = tid; t < p.M - 1; t += Q::THREADS) st[t] = x[p.n - (p.M - 1) + t];
-        }
-        pair_phase_c1<REAL>(kappa, tlane, s, r, hi_s, wr_s, peer_recv);
-        tmem_fence_before_sync();
-        cluster_sync();  // the other CTA's P values have landed in bufs
-        tmem_fence_after_sync();
-        pair_phase_c2a<REAL>(p, lu, chan<REAL>(p, chu).y, un < uend ? lun : -1, chan<REAL>(p, chn), kappa, tlane,
-                             s, r, hi_s, wr_s, bufs);
-        chu = chn;
-        lu = lun;
-    }
+    if (kappa == 0)
+        pair_loop<REAL, MULTI, 0>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1, peer_recv,
+                                  gbar);
+    else
+        pair_loop<REAL, MULTI, 1>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1, peer_recv,
+                                  gbar);
 
     tmem_fence_before_sync();
     __syncthreads();

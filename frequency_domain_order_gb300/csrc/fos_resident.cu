@@ -73,7 +73,7 @@ template <int LOGN, bool REAL>
 __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void *yc, int64_t ua, const Chan &cha,
                                          uint32_t tlane, int s, int r, const float2 *hi_s, const float2 *wr_s) {
     using R_ = ResidentCfg<LOGN, REAL>;
-    constexpr int C = R_::C, P = R_::P, HI = R_::HI;
+    constexpr int C = R_::C, P = R_::P;
     // uc, ua: unit indices within their channels; yc: uc's channel's output, cha: ua's channel
     const int64_t sc = (REAL ? 2 * uc : uc) * p.L - (p.M - 1);  // output index of R[0] of unit uc
     const bool whole = sc + R_::N + (REAL ? p.L : 0) <= p.n;
@@ -82,9 +82,7 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
     const int lim = p.n - sc > (int64_t)R_::N + p.L ? R_::N + p.L : (int)(p.n - sc);
     const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
     const bool interior = sa >= 0 && sa + R_::N + (REAL ? p.L : 0) <= p.n;
-    float2 wr[C];
-#pragma unroll
-    for (int c = 1; c < C; ++c) wr[c] = wr_s[c * 128 + r];
+    const float2 wr1 = wr_s[128 + r];  // W_N^r
 #pragma unroll 1
     for (int st = 0; st < 4; ++st) {
         const int i0 = (st & 1) + 4 * (st >> 1);  // 0, 1, 4, 5: steps i0 and i0 + 2
@@ -105,8 +103,10 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int m = 8 * s + i0 + 2 * h;
+                float2 w[C];  // W_N^{bc}: W_N^b = W_N^r W_N^{128 m} (m < 32 < N / 128), then its powers
+                twiddle_powers<C>(cmul(wr1, hi_s[m]), w);
 #pragma unroll
-                for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+                for (int c = 1; c < C; ++c) v[h][c] = cmulc(v[h][c], w[c]);
                 dft<C, +1>(v[h]);
                 const int b = r + 128 * m;
                 // y[sc + b + P a] at a constant offset from one pointer (dereferenced only for t >= keep)
@@ -130,8 +130,10 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
             for (int h = 0; h < 2; ++h) {
                 const int m = 8 * s + i0 + 2 * h;
                 dft<C, -1>(xa[h]);
+                float2 w[C];
+                twiddle_powers<C>(cmul(wr1, hi_s[m]), w);
 #pragma unroll
-                for (int c = 1; c < C; ++c) xa[h][c] = cmul(xa[h][c], cmul(wr[c], hi_s[(m * c) & (HI - 1)]));
+                for (int c = 1; c < C; ++c) xa[h][c] = cmul(xa[h][c], w[c]);
             }
 #pragma unroll
             for (int c = 0; c < C; ++c) tmem_st4(tlane + 64u * c + col, xa[0][c], xa[1][c]);
@@ -194,7 +196,9 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
         const int64_t un = u + gridDim.x;
         const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, chan<REAL>(p, chn), lun, tid);
-        phase_b<R_::C>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
+        // (the packed quarter turn in the P-point transforms: C3 -2.3% measured; the pair kernel
+        // keeps the scalar form, +2.4% otherwise)
+        phase_b<R_::C, true>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();

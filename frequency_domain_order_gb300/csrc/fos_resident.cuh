@@ -12,6 +12,28 @@
 
 namespace fos {
 
+// w[c] = g^c for c = 1 .. C-1 (C = 4, 8 or 16; w[0] is not written): the twiddles W_N^{bc} of
+// one point set from g = W_N^b, by squarings and products, so that no power is more than four
+// complex multiplications from g.
+template <int C>
+__device__ __forceinline__ void twiddle_powers(float2 g, float2 (&w)[C]) {
+    static_assert(C == 4 || C == 8 || C == 16, "C-point stages of 4, 8 or 16");
+    w[1] = g;
+    w[2] = cmul(g, g);
+    w[3] = cmul(w[2], g);
+    if constexpr (C > 4) {
+        w[4] = cmul(w[2], w[2]);
+        w[5] = cmul(w[4], g);
+        w[6] = cmul(w[4], w[2]);
+        w[7] = cmul(w[4], w[3]);
+    }
+    if constexpr (C > 8) {
+        w[8] = cmul(w[4], w[4]);
+#pragma unroll
+        for (int c = 9; c < 16; ++c) w[c] = cmul(w[8], w[c - 8]);
+    }
+}
+
 // Complex slot pair of steps i0 and i0 + 2 of thread row s: columns of q(c, 8 s + i0) and
 // q(c, 8 s + i0 + 2) = that + 1, relative to c's 64 columns.
 __device__ __forceinline__ uint32_t step_col(int s, int i0) {
@@ -101,7 +123,7 @@ __device__ __forceinline__ void prefetch_window(const BlockParams &p, const Chan
 // Phase B: P-point FFT, multiply by H, inverse FFT for the CL local sub-transforms
 // c' = g, g + 2, ... (Tensor Memory columns 64 c'), whose bins are H[c + C d] with
 // c = hoff + hstride c'.  col0 = 32 (j >> 7), passed in by the caller as a warp-uniform value.
-template <int CL>
+template <int CL, bool PQ = false>
 __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
                                         float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar, int hoff,
                                         int hstride, uint32_t col0) {
@@ -121,14 +143,14 @@ __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, in
                 v[8 + e] = make_float2(f1[2 * e], f1[2 * e + 1]);
             }
         }
-        fft_tm<LOGP, 256, false>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, false, PQ>(v, b0, b1, stw, 0u, j, gbar);
         const float2 *hp = p.H + (hoff + hstride * c) * P + j;
         float2 h[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) h[e] = __ldg(hp + 256 * e);
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], h[e]);
-        fft_tm<LOGP, 256, true>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, true, PQ>(v, b0, b1, stw, 0u, j, gbar);
         {
             float f0[16], f1[16];
 #pragma unroll
