@@ -383,6 +383,8 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int, cpu_budget:
         kind = fir_os.COEF_TIME
     plan = fir_os.Plan(w.M, w.N, coef, real=w.real, coef_kind=kind)
     plan_ms = plan_time(fir_os, w, coef, kind)
+    if args.dft_engine == "tensor":
+        plan.set_dft_engine(fir_os.DFT_TENSOR)
     sets = buffer_sets(2 * x.nbytes)
     xs = [torch.from_numpy(x).to(dev) for _ in range(sets)]
     ys = [torch.empty_like(xs[0]) for _ in range(sets)]
@@ -541,7 +543,7 @@ def run_ours(args, w: W.Workload, world: int, rank: int, local: int, cpu_budget:
                         f"replayed {len(runs)} times; per-step median and p20 are over replays"
                         if graphs is not None else "direct launches"),
         "clocks": clk,
-        "kernel": plan.kernel(),
+        "kernel": dict(plan.kernel(), dft_engine=args.dft_engine),
         "plan_ms": plan_ms,
         "wall_s_timed_region": wall,
     }
@@ -868,6 +870,8 @@ def main(argv=None):
     ap.add_argument("--also", default=None,
                     help="comma-separated further workloads measured in the same run and reported under "
                          f"'also' (default: {','.join(DEFAULT_ALSO)} with the default workload, else none)")
+    ap.add_argument("--dft-engine", choices=["fp32", "tensor"], default="fp32",
+                    help="16-point DFTs as float32 butterflies (default) or on the tensor cores (N = 4096 only)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="shorten a single-call workload to this many blocks (smaller profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=50)

@@ -285,6 +285,8 @@ struct fir_os_plan {
     float2 *d_twa = nullptr;
     int *d_err = nullptr;
     uint64_t wait_ns = fos::kWaitLimitNs;  // limit of a kernel's wait for one bulk copy
+    int dft_engine = FIR_OS_DFT_FP32;      // FIR_OS_DFT_TENSOR: the tensor-core kernel variant
+    float2 *d_btc = nullptr;               // its split 16-point DFT matrices (fos_tc.cuh)
     // host-buffer path (lazily created)
     int64_t host_chunk = 0;
     void *hx[2] = {nullptr, nullptr};
@@ -345,6 +347,7 @@ void free_plan(fir_os_plan *p) {
     dev_free(p->d_tw);
     dev_free(p->d_twa);
     dev_free(p->d_err);
+    dev_free(p->d_btc);
     release_host_path(p);
     alloc_give(p);
 }
@@ -418,6 +421,7 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     bp.twa = p->d_twa;
     bp.err = p->d_err;
     bp.wait_ns = p->wait_ns;
+    bp.btc = p->d_btc;
     bp.n = n;
     bp.upc = units_for(p, n);
     bp.nunits = bp.upc * channels;
@@ -458,7 +462,10 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     // less than one wave: each group filters one unit at most, so the per-thread Tensor Memory
     // set-up of the plan constants would sit on the call's critical path; the variant that keeps
     // them in shared memory avoids it
-    if (p->kernel.func_short && bp.nunits < (int64_t)p->max_units_in_flight * p->kernel.groups) {
+    if (p->dft_engine == FIR_OS_DFT_TENSOR) {
+        func = p->kernel.func_tc;
+        cfg.dynamicSmemBytes = (size_t)p->kernel.smem_tc;
+    } else if (p->kernel.func_short && bp.nunits < (int64_t)p->max_units_in_flight * p->kernel.groups) {
         func = p->kernel.func_short;
         cfg.dynamicSmemBytes = (size_t)p->kernel.smem_short;
     }
@@ -803,6 +810,57 @@ int fir_os_plan_set_wait_limit(fir_os_plan_t plan, int64_t limit_ns) {
     if (limit_ns < 0 || limit_ns > 60LL * 1000000000LL)
         return fail(FIR_OS_E_INVAL, "wait limit %lld ns is outside [0, 60 s]", (long long)limit_ns);
     plan->wait_ns = (uint64_t)limit_ns;
+    return FIR_OS_OK;
+}
+
+int fir_os_plan_set_dft_engine(fir_os_plan_t plan, int engine) {
+    if (!plan) return fail(FIR_OS_E_INVAL, "plan is NULL");
+    if (engine != FIR_OS_DFT_FP32 && engine != FIR_OS_DFT_TENSOR)
+        return fail(FIR_OS_E_INVAL, "engine %d is neither FIR_OS_DFT_FP32 nor FIR_OS_DFT_TENSOR", engine);
+    if (engine == FIR_OS_DFT_TENSOR && !plan->kernel.func_tc)
+        return fail(FIR_OS_E_UNSUPPORTED, "the tensor-core DFT engine exists for N = 4096 only (N = %d)", plan->N);
+    if (engine == FIR_OS_DFT_TENSOR && !plan->d_btc) {
+        int rc = check_device(plan);
+        if (rc) return rc;
+        // B[c][k], c = 2m + output component, k = 2e + input component, of the 16-point DFT
+        // sum_e v[e] W^{em} with W = e^{dir 2 pi i / 16}, split into a TF32 part (low 13 mantissa
+        // bits cleared) and the float32 rest, from float64 values; laid out as the tensor cores
+        // read a K-major tile (fos_tc.cuh): forward hi, forward lo, inverse hi, inverse lo
+        const int per = (int)(fos::kTcBTileBytes / 4);
+        std::vector<float> tab((size_t)4 * per, 0.f);
+        for (int d = 0; d < 2; ++d) {
+            const double dir = d == 0 ? -1.0 : 1.0;
+            for (int c = 0; c < 32; ++c)
+                for (int k = 0; k < 32; ++k) {
+                    const int m = c >> 1, e = k >> 1;
+                    const double ang = 2.0 * M_PI * (double)((e * m) % 16) / 16.0;
+                    const double cs = std::cos(ang), sn = dir * std::sin(ang);
+                    const double val = (c & 1) == 0 ? ((k & 1) == 0 ? cs : -sn) : ((k & 1) == 0 ? sn : cs);
+                    float hi = (float)val;
+                    uint32_t bits;
+                    std::memcpy(&bits, &hi, 4);
+                    bits &= 0xFFFFE000u;
+                    std::memcpy(&hi, &bits, 4);
+                    const float lo = (float)(val - (double)hi);
+                    const uint32_t off = fos::tc_offset(c, k) / 4;
+                    tab[(size_t)(2 * d) * per + off] = hi;
+                    tab[(size_t)(2 * d + 1) * per + off] = lo;
+                }
+        }
+        DeviceScope on(plan->device);
+        cudaError_t e = dev_alloc(&plan->d_btc, sizeof(float) * tab.size());
+        if (e != cudaSuccess) return alloc_fail(e, "cudaMalloc(tensor-core DFT matrices)");
+        if ((e = cudaMemcpy(plan->d_btc, tab.data(), sizeof(float) * tab.size(), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+            dev_free(plan->d_btc);
+            plan->d_btc = nullptr;
+            return cuda_fail(e, "tensor-core DFT matrix upload");
+        }
+        if ((e = cudaFuncSetAttribute(plan->kernel.func_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      plan->kernel.smem_tc)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(smem, tensor-core variant)");
+    }
+    plan->dft_engine = engine;
     return FIR_OS_OK;
 }
 

@@ -82,6 +82,17 @@ struct BlockCfg {
     // memory after the buffers (no Tensor Memory): for N <= 1024 they fit beside them
     static constexpr int SMC_BYTES = 8 * (N + S::TW_ENTRIES);
     static constexpr bool HAS_SMC = SMEM_BYTES + SMC_BYTES <= 227 * 1024;
+    // the tensor-core variant (N = 4096): the four 4 KB DFT-matrix tiles after the header, then
+    // per group [staging 0][exchange][staging 1], so that the exchange buffer and whichever
+    // staging window is being filtered are adjacent: the group's 64 KB of A tiles span the two
+    static constexpr bool HAS_TC = (LOGN == 12);
+    static constexpr int TC_B_OFF = HDR_BYTES;
+    static constexpr int TC_GROUP_OFF = HDR_BYTES + 4 * (int)kTcBTileBytes;
+    static constexpr int SMEM_TC = TC_GROUP_OFF + GROUPS * 3 * BUF_BYTES;
+    static_assert(!HAS_TC || (2 * BUF_BYTES >= 4 * (int)kTcTileBytes && T == 256 && F == 1 &&
+                              TM_NEED <= 384 && TM_COLS == 512 && SMEM_TC <= 227 * 1024 &&
+                              16 + 24 * GROUPS <= HDR_BYTES),
+                  "tensor-core variant layout");
     using Bar = GroupBarrier<GT>;
 };
 
@@ -247,7 +258,8 @@ __device__ __forceinline__ void write_state(const BlockParams &p, const Chan &ch
 
 // SMC: H / N and the twiddles in shared memory instead of Tensor Memory (calls of less than one
 // wave, where the per-thread Tensor Memory set-up is on every call's critical path)
-template <int LOGN, bool REAL, bool SMC>
+// TC: the 16-point DFTs of every pass on the tensor cores (N = 4096 only; fos_tc.cuh)
+template <int LOGN, bool REAL, bool SMC, bool TC = false>
 __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, REAL>::MIN_BLOCKS)
     fos_block_kernel(const BlockParams p) {
     using C = BlockCfg<LOGN, REAL>;
@@ -264,10 +276,13 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     const int j = tg % T;           // thread within the transform
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 16) + 2 * g;
     uint32_t *tm_base_slot = reinterpret_cast<uint32_t *>(smem);
-    unsigned char *gbase = smem + C::HDR_BYTES + g * 3 * C::BUF_BYTES;
-    float2 *xbuf = reinterpret_cast<float2 *>(gbase);  // exchange buffer
-    unsigned char *stg0 = gbase + C::BUF_BYTES;
+    unsigned char *gbase = smem + (TC ? C::TC_GROUP_OFF : C::HDR_BYTES) + g * 3 * C::BUF_BYTES;
+    // exchange buffer and the two staging windows (the tensor-core variant puts the exchange
+    // buffer between the windows)
+    float2 *xbuf = reinterpret_cast<float2 *>(gbase + (TC ? C::BUF_BYTES : 0));
+    unsigned char *stg0 = gbase + (TC ? 0 : C::BUF_BYTES);
     unsigned char *stg1 = gbase + 2 * C::BUF_BYTES;
+    uint64_t *tcbar = reinterpret_cast<uint64_t *>(smem + 16 + 16 * C::GROUPS) + g;  // TC: MMA completion
     const typename C::Bar gbar{1 + g};
 
     griddep_launch_dependents();  // the next call's kernel may start its own set-up
@@ -278,7 +293,13 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     if (tg == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        if (TC) mbar_init(tcbar, 1);
         fence_mbar_init();
+    }
+    if constexpr (TC) {  // the split DFT matrices, read by the tensor cores (async proxy)
+        copy_table(p.btc, reinterpret_cast<float2 *>(smem + C::TC_B_OFF), 4 * (int)kTcBTileBytes / 8, tid,
+                   C::THREADS);
+        fence_proxy_async_smem();
     }
     tmem_fence_before_sync();
     __syncthreads();
@@ -306,9 +327,21 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
     }
 
     // this thread's TMEM columns: lane 32 (warp % 4) + (tid % 32), columns from slot * 32 NPASS
-    const uint32_t tma = SMC ? 0u
-                             : __shfl_sync(0xffffffffu, *tm_base_slot, 0) +
-                                   ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+    const uint32_t tm0 = SMC ? 0u : __shfl_sync(0xffffffffu, *tm_base_slot, 0);
+    const uint32_t tma = SMC ? 0u : tm0 + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * C::TM_COLS_THREAD);
+    // TC: the group's two 128-row accumulators in columns 384 + 64 g (+ 32); thread j's row is
+    // j mod 128 of tile j / 128, which is its own lane
+    TcCtx tc{};
+    uint32_t tcpar = 0u;
+    if constexpr (TC) {
+        tc.b_base = smem_addr(smem + C::TC_B_OFF);
+        tc.d_tile = tm0 + 384u + 64u * (uint32_t)g;
+        tc.d_row = tm0 + ((uint32_t)(32 * (warp & 3)) << 16) + 384u + 64u * (uint32_t)g + 32u * (uint32_t)(j >> 7);
+        tc.row_off = (uint32_t)(j >> 7) * 2u * kTcTileBytes + tc_offset(j & 127, 0);
+        tc.mbar = tcbar;
+        tc.err = p.err;
+        tc.leader = tg == 0;
+    }
     float2 *cH = reinterpret_cast<float2 *>(smem + C::SMEM_BYTES);  // SMC: H / N, then the twiddles
     float2 *cT = cH + C::N;
     if constexpr (SMC) {
@@ -408,7 +441,10 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
         // step 4: FFT, multiply by H, IFFT.  Exchange buffers: xbuf and (once read) cur.
         float2 *b0 = xbuf + f * xpad_len(C::N);
         float2 *b1 = reinterpret_cast<float2 *>(cur) + f * xpad_len(C::N);
-        fft_tm<LOGN, SMC ? (1 << 30) : 0, false>(v, b0, b1, cT, tma, j, gbar);
+        if constexpr (TC)  // the A tiles span the exchange buffer and `cur`, whichever comes first
+            tc.a_base = smem_addr(cur < reinterpret_cast<unsigned char *>(xbuf) ? cur
+                                                                               : reinterpret_cast<unsigned char *>(xbuf));
+        fft_tm<LOGN, SMC ? (1 << 30) : 0, false, false, TC>(v, b0, b1, cT, tma, j, gbar, &tc, &tcpar);
         if constexpr (SMC) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], cH[j + e * T]);
@@ -423,7 +459,7 @@ __global__ void __launch_bounds__(BlockCfg<LOGN, REAL>::THREADS, BlockCfg<LOGN, 
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[8 + e] = cmul(v[8 + e], make_float2(h[2 * e], h[2 * e + 1]));
         }
-        fft_tm<LOGN, SMC ? (1 << 30) : 0, true>(v, b0, b1, cT, tma, j, gbar);
+        fft_tm<LOGN, SMC ? (1 << 30) : 0, true, false, TC>(v, b0, b1, cT, tma, j, gbar, &tc, &tcpar);
 
         // step 5: drop R[0 .. M-2], store R[M-1 .. N) as Y_i
         const int64_t blk = REAL ? 2 * (lu * C::F + f) : (lu * C::F + f);
@@ -491,6 +527,10 @@ KernelEntry block_entry() {
     if constexpr (C::HAS_SMC) {
         k.func_short = reinterpret_cast<const void *>(&fos_block_kernel<LOGN, REAL, true>);
         k.smem_short = C::SMEM_BYTES + C::SMC_BYTES;
+    }
+    if constexpr (C::HAS_TC) {
+        k.func_tc = reinterpret_cast<const void *>(&fos_block_kernel<LOGN, REAL, false, true>);
+        k.smem_tc = C::SMEM_TC;
     }
     k.threads = C::THREADS;
     k.smem = C::SMEM_BYTES;

@@ -16,6 +16,7 @@
 #pragma once
 
 #include "fos_device.cuh"
+#include "fos_tc.cuh"
 
 namespace fos {
 
@@ -71,9 +72,10 @@ struct TwLayout {
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
 // transform's last pass reads.  Every buffer is xpad_len(N) elements of this transform.
 
-template <int LOGN, int SMAX, int P, bool INV, bool PQ, class Bar>
+template <int LOGN, int SMAX, int P, bool INV, bool PQ, bool TC, class Bar>
 __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
-                                            uint32_t tm, int j, const Bar &bar) {
+                                            uint32_t tm, int j, const Bar &bar, const TcCtx *tc,
+                                            uint32_t *tcpar) {
     using S = FftShape<LOGN>;
     if constexpr (P < S::NPASS) {
         constexpr int T = S::T;
@@ -108,7 +110,8 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
 #pragma unroll
             for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
         }
-        dft<16, DIR, PQ>(v);
+        if constexpr (TC) tc_dft16<DIR>(v, *tc, bar, *tcpar);
+        else dft<16, DIR, PQ>(v);
         if constexpr (!last) {
             const int base = (j / Ns) * (16 * Ns) + m;
             if constexpr (Ns % 16 == 0) {
@@ -121,29 +124,36 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ>(v, b0, b1, stw, tm, j, bar);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ, TC>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
     }
 }
 
 // Transform v in place (layout z[j + e T] -> Z[j + e T]).  `bar` synchronises the threads that
 // share the two buffers.  No barrier is needed before the first write: see the buffer rotation
 // above and the callers' barrier placement.  PQ: the quarter-turn form of dft4 (fos_device.cuh).
-template <int LOGN, int SMAX, bool INV, bool PQ = false, class Bar>
+// TC: every radix-16 DFT on the tensor cores (fos_tc.cuh; tc and tcpar are then the group's
+// context and MMA-barrier phase, and the tile region may overlap b0 and b1).
+template <int LOGN, int SMAX, bool INV, bool PQ = false, bool TC = false, class Bar>
 __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
-                                       int j, const Bar &bar) {
+                                       int j, const Bar &bar, const TcCtx *tc = nullptr,
+                                       uint32_t *tcpar = nullptr) {
     using S = FftShape<LOGN>;
     constexpr int T = S::T, R0 = S::R0, G = 16 / R0;
     constexpr int DIR = INV ? 1 : -1;
     constexpr int SH = INV ? S::NPASS + 1 : 0;
     float2 *wr = (SH % 2 == 0) ? b0 : b1;
+    if constexpr (TC && R0 == 16) {
+        tc_dft16<DIR>(v, *tc, bar, *tcpar);
+    } else {
 #pragma unroll
-    for (int q = 0; q < G; ++q) {
-        float2 a[R0];
+        for (int q = 0; q < G; ++q) {
+            float2 a[R0];
 #pragma unroll
-        for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
-        dft<R0, DIR, PQ>(a);
+            for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
+            dft<R0, DIR, PQ>(a);
 #pragma unroll
-        for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
+            for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
+        }
     }
     if constexpr ((T * R0) % 16 == 0) {
         float2 *dst = wr + j * R0 + ((j * R0) >> 4);
@@ -158,7 +168,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, SMAX, 1, INV, PQ>(v, b0, b1, stw, tm, j, bar);
+    fft_tm_pass<LOGN, SMAX, 1, INV, PQ, TC>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
 }
 
 }  // namespace fos

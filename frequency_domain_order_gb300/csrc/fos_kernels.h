@@ -16,6 +16,8 @@ struct BlockParams {
     const float2 *tw;      // Stockham pass twiddles of the per-CTA transform
     const float2 *twa;     // resident / pair kernels: W_N^{r c} at [c * 128 + r] (c < C),
                            // then W_N^{128 k} at [C * 128 + k] (k < N / 128)
+    const float2 *btc;     // tensor-core variant: the split 16-point DFT matrices (fos_tc.cuh),
+                           // forward hi, forward lo, inverse hi, inverse lo, 4 KB each
     int *err;              // device error word (set to 1 when a bounded wait ran out)
     uint64_t wait_ns;      // limit of one bounded wait for a bulk copy (0: every wait runs out)
     int64_t n;             // samples in this call (per channel)
@@ -67,6 +69,8 @@ struct KernelEntry {
     const void *func_multi = nullptr;  // the same for calls of more than one channel, if separate
     const void *func_short = nullptr;  // the variant for calls of less than one wave, if any
     int smem_short = 0;                // its dynamic shared memory per CTA (bytes)
+    const void *func_tc = nullptr;     // the variant with its 16-point DFTs on the tensor cores, if any
+    int smem_tc = 0;                   // its dynamic shared memory per CTA (bytes)
     int threads = 0;             // threads per CTA
     int smem = 0;                // dynamic shared memory per CTA (bytes)
     int cluster = 1;             // CTAs per cluster (1 = no cluster)

@@ -28,6 +28,8 @@ REAL = 0
 COMPLEX = 1
 COEF_TIME = 0
 COEF_FREQ = 1
+DFT_FP32 = 0
+DFT_TENSOR = 1
 
 # every entry point include/fir_os.h declares, with its ctypes signature
 _P, _I, _I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
@@ -42,6 +44,7 @@ SIGNATURES = {
                                 ctypes.POINTER(_I)]),
     "fir_os_device_status": (_I, [_P, _P]),
     "fir_os_plan_set_wait_limit": (_I, [_P, _I64]),
+    "fir_os_plan_set_dft_engine": (_I, [_P, _I]),
     "fir_os_debug_fail_alloc": (_I, [_I]),
     "fir_os_debug_live_allocs": (_I64, []),
     "fir_os_launches": (_I, [_P, _I64]),
@@ -217,6 +220,10 @@ class Plan:
 
     def device_status(self, stream=None):
         _check(lib().fir_os_device_status(self._h, _stream_handle(stream)))
+
+    def set_dft_engine(self, engine: int):
+        """fir_os_plan_set_dft_engine: DFT_FP32 (default) or DFT_TENSOR (N = 4096 only)."""
+        _check(lib().fir_os_plan_set_dft_engine(self._h, int(engine)))
 
     def set_wait_limit(self, limit_ns: int):
         """fir_os_plan_set_wait_limit: the kernels' limit for one bulk-copy wait (0: every wait

@@ -195,6 +195,22 @@ int fir_os_device_status(fir_os_plan_t plan, void *stream);
  * enqueued after the call.  FIR_OS_E_INVAL for a NULL plan or a limit outside [0, 60 s]. */
 int fir_os_plan_set_wait_limit(fir_os_plan_t plan, int64_t limit_ns);
 
+/* fir_os_plan_set_dft_engine -- how the 16-point DFTs of the plan's radix-16 transform passes
+ * (step 4 of the claim: the FFT and IFFT of every block) are computed:
+ *   FIR_OS_DFT_FP32    (default) as butterflies in float32 registers;
+ *   FIR_OS_DFT_TENSOR  as matrix products on the tensor cores: 128 vectors per tcgen05.mma tile,
+ *                      TF32 operands split into a TF32 part and the float32 rest (three products,
+ *                      float32 accumulation in Tensor Memory), the twiddles still in float32.
+ * The tensor engine exists for N = 4096 only (FIR_OS_E_UNSUPPORTED otherwise); it is an
+ * option, off by default.  Its outputs meet the same parity bar but are not bitwise equal to
+ * the default's.  The first
+ * FIR_OS_DFT_TENSOR call allocates and uploads the 16 KB of split DFT matrices (synchronous;
+ * FIR_OS_E_NOMEM if that allocation fails).  Applies to launches enqueued after the call.
+ * FIR_OS_E_INVAL for a NULL plan or an unknown engine. */
+#define FIR_OS_DFT_FP32 0
+#define FIR_OS_DFT_TENSOR 1
+int fir_os_plan_set_dft_engine(fir_os_plan_t plan, int engine);
+
 /* fir_os_debug_fail_alloc -- make the k-th next allocation of the library (its plan objects
  * and the device buffers of fir_os_plan_create, fir_chan_plan_create and the first
  * fir_os_execute_host call) fail as if memory had run out, without asking CUDA; k = 0

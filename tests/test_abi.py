@@ -88,6 +88,7 @@ def test_no_device_is_an_error_not_a_crash(L):
 
 def test_test_hooks_reject_bad_arguments(L):
     assert L.fir_os_plan_set_wait_limit(None, 0) == fir_os.E_INVAL
+    assert L.fir_os_plan_set_dft_engine(None, fir_os.DFT_TENSOR) == fir_os.E_INVAL
     assert L.fir_os_debug_fail_alloc(-1) == fir_os.E_INVAL
     assert L.fir_os_debug_fail_alloc(0) == fir_os.OK
 

@@ -1,0 +1,131 @@
+"""The tensor-core DFT engine (fir_os_plan_set_dft_engine, FIR_OS_DFT_TENSOR) against the oracle.
+
+With it every radix-16 pass of the N = 4096 block transforms (step 4 of the claim in
+"一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法", 主权项) computes its 16-point DFTs as
+tcgen05.mma matrix products on split TF32 operands.  The outputs must meet the same parity bar
+as the float32 engine (relative L2 error <= 1e-5, max abs error <= 1e-4 * ||h||_1 * max|x|,
+measured in float64): whole streams with ragged tails, several calls with the state carried,
+complex and packed real data, the full C2 workload sampled, and M = 1 and M = N.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import assert_parity, make_plan, run_calls, run_device, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fo():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from frequency_domain_order_gb300 import build, fir_os
+    build.build()
+    return fir_os
+
+
+def _tensor_plan(fo, w):
+    plan = make_plan(w)
+    plan.set_dft_engine(fo.DFT_TENSOR)
+    return plan
+
+
+@pytest.mark.parametrize("real", [False, True])
+@pytest.mark.parametrize("blocks,tail,calls", [(1, 0, 1), (7, 1000, 1), (600, 333, 3), (3000, 5, 1)])
+def test_tensor_engine_against_oracle(fo, real, blocks, tail, calls):
+    base = W.WORKLOADS["C2"]
+    if real:  # C2's filter on real data
+        base = W.Workload("C2real", True, base.M, base.N, base.calls, 11, "time", base.h_kind, base.h_args)
+    w = W.scaled(base, blocks, tail, calls)
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    plan = _tensor_plan(fo, w)
+    y, st = run_calls(plan, x, w.calls)
+    if w.n <= 400_000:
+        want, s_want = oracle.direct(x, h)
+        assert_parity(y, want, h, x, f"{w.name} tensor engine")
+    else:
+        idx = W.sample_indices(w.n, w.L, seed=blocks, n_random=1 << 14)
+        want = oracle.direct_at(x, h, None, idx)
+        assert_parity(y[idx], want, h, x, f"{w.name} tensor engine, sampled")
+        s_want = oracle.state_next(x, None, w.M)
+    assert np.array_equal(st, (s_want.real if real else s_want).astype(st.dtype))
+    plan.close()
+
+
+@pytest.mark.parametrize("M", [1, 4096, 2049])
+def test_tensor_engine_extreme_taps(fo, M):
+    rng = np.random.Generator(np.random.PCG64(M))
+    N = 4096
+    n = 5 * (N - M + 1) + 77
+    x = (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(np.complex64)
+    h = ((rng.standard_normal(M) + 1j * rng.standard_normal(M)) / np.sqrt(M)).astype(np.complex64)
+    s0 = (rng.standard_normal(M - 1) + 1j * rng.standard_normal(M - 1)).astype(np.complex64)
+    plan = fo.Plan(M, N, to_dev(h))
+    plan.set_dft_engine(fo.DFT_TENSOR)
+    y, st = run_calls(plan, x, (n,), s0 if M > 1 else None)
+    want, s_want = oracle.direct(x, h.astype(np.complex128), s0 if M > 1 else None)
+    assert_parity(y, want, h, x, f"M={M} tensor engine")
+    if M > 1:
+        assert np.array_equal(st, s_want.astype(np.complex64))
+    plan.close()
+
+
+def test_tensor_engine_full_c2_sampled_and_close_to_fp32(fo):
+    import torch
+    w = W.WORKLOADS["C2"]
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    xd = to_dev(x)
+    plan = make_plan(w)
+    y32, _ = run_device(plan, xd, w.calls)
+    plan.set_dft_engine(fo.DFT_TENSOR)
+    ytc, _ = run_device(plan, xd, w.calls)
+    idx = W.sample_indices(w.n, w.L, seed=5, n_random=1 << 15)
+    want = oracle.direct_at(x, h, None, idx)
+    got = ytc.cpu().numpy()
+    assert_parity(got[idx], want, h, x, "C2 tensor engine, sampled")
+    # the two engines agree to the parity bar with each other over every output
+    assert_parity(got, y32.cpu().numpy(), h, x, "tensor vs float32 engine")
+    # and switching back gives the float32 engine's outputs bit for bit
+    plan.set_dft_engine(fo.DFT_FP32)
+    yb, _ = run_device(plan, xd, w.calls)
+    assert torch.equal(yb.view(torch.int32), y32.view(torch.int32))
+    plan.close()
+
+
+def test_tensor_engine_only_for_4096(fo):
+    for name in ("C1", "C3"):
+        plan = make_plan(W.scaled(W.WORKLOADS[name], 2))
+        with pytest.raises(fo.FirOsError) as err:
+            plan.set_dft_engine(fo.DFT_TENSOR)
+        assert err.value.status == fo.E_UNSUPPORTED
+        with pytest.raises(fo.FirOsError) as err:
+            plan.set_dft_engine(7)
+        assert err.value.status == fo.E_INVAL
+        plan.close()
+
+
+def test_tensor_engine_with_the_wait_fallback(fo):
+    """The zero wait limit (every bulk-copy wait runs out) with the tensor engine: the plain-load
+    fallback gathers into the window the tiles overlap; outputs still meet the bar."""
+    w = W.scaled(W.WORKLOADS["C2"], 300, 17)
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    plan = _tensor_plan(fo, w)
+    plan.set_wait_limit(0)
+    xd = to_dev(x)
+    import torch
+    yd = torch.empty_like(xd)
+    st = torch.zeros(w.M - 1, dtype=xd.dtype, device="cuda")
+    plan.execute(xd, yd, st)
+    torch.cuda.synchronize()
+    with pytest.raises(fo.FirOsError) as err:
+        plan.device_status()
+    assert err.value.status == fo.E_DEVICE
+    want, _ = oracle.direct(x, h)
+    assert_parity(yd.cpu().numpy(), want, h, x, "tensor engine, fallback gathers")
+    plan.close()
