@@ -506,28 +506,28 @@ struct BlockCost {
     double sm_us[3];  // at L/N = 1/4, 1/2, 3/4
 };
 const BlockCost kBlockCost[] = {
-    {64, 0, {0.0315, 0.0340, 0.0370}},
-    {128, 0, {0.0472, 0.0501, 0.0535}},
-    {256, 0, {0.0870, 0.0912, 0.0968}},
-    {512, 0, {0.2358, 0.2461, 0.2554}},
-    {1024, 0, {0.4808, 0.5014, 0.5196}},
-    {2048, 0, {1.0836, 1.1166, 1.1668}},
-    {4096, 0, {2.4637, 2.5038, 2.6723}},
-    {8192, 0, {6.5200, 6.9616, 7.4397}},
-    {16384, 0, {14.7463, 16.0497, 17.3581}},
-    {32768, 0, {28.5274, 31.8075, 36.5530}},
-    {65536, 0, {78.5992, 82.8704, 92.8540}},
-    {64, 1, {0.0204, 0.0226, 0.0256}},
-    {128, 1, {0.0274, 0.0296, 0.0320}},
-    {256, 1, {0.0468, 0.0494, 0.0524}},
-    {512, 1, {0.1193, 0.1246, 0.1310}},
-    {1024, 1, {0.2464, 0.2557, 0.2689}},
-    {2048, 1, {0.6023, 0.6139, 0.6199}},
-    {4096, 1, {1.2270, 1.2844, 1.3675}},
-    {8192, 1, {3.3370, 3.5279, 3.7678}},
-    {16384, 1, {7.3716, 8.2430, 9.0462}},
-    {32768, 1, {15.2068, 17.3128, 20.4274}},
-    {65536, 1, {42.8199, 45.2291, 51.0948}},
+    {64, 0, {0.0309, 0.0330, 0.0357}},
+    {128, 0, {0.0460, 0.0484, 0.0513}},
+    {256, 0, {0.0858, 0.0893, 0.0931}},
+    {512, 0, {0.2290, 0.2354, 0.2434}},
+    {1024, 0, {0.4600, 0.4732, 0.4841}},
+    {2048, 0, {1.0472, 1.0486, 1.0733}},
+    {4096, 0, {2.3304, 2.3415, 2.4525}},
+    {8192, 0, {6.4839, 6.7751, 7.1168}},
+    {16384, 0, {12.2143, 12.7163, 13.1371}},
+    {32768, 0, {23.9522, 24.8781, 26.2362}},
+    {65536, 0, {61.0155, 63.3709, 65.2650}},
+    {64, 1, {0.0206, 0.0229, 0.0259}},
+    {128, 1, {0.0278, 0.0301, 0.0327}},
+    {256, 1, {0.0472, 0.0502, 0.0534}},
+    {512, 1, {0.1212, 0.1277, 0.1344}},
+    {1024, 1, {0.2384, 0.2499, 0.2649}},
+    {2048, 1, {0.5367, 0.5664, 0.5943}},
+    {4096, 1, {1.2849, 1.2285, 1.3766}},
+    {8192, 1, {3.3923, 3.5429, 3.7589}},
+    {16384, 1, {6.4027, 6.7892, 7.1268}},
+    {32768, 1, {12.8559, 14.3569, 15.0027}},
+    {65536, 1, {31.5299, 34.3959, 35.3792}},
 };
 
 // Predicted throughput (output samples per second, 1e9) of an (M, N) plan on `sms` SMs: L
