@@ -72,7 +72,7 @@ struct TwLayout {
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
 // transform's last pass reads.  Every buffer is xpad_len(N) elements of this transform.
 
-template <int LOGN, int SMAX, int P, bool INV, bool PQ, bool TC, class Bar>
+template <int LOGN, int SMAX, int P, bool INV, bool PQ, bool TC, bool FS, class Bar>
 __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
                                             uint32_t tm, int j, const Bar &bar, const TcCtx *tc,
                                             uint32_t *tcpar) {
@@ -111,7 +111,7 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             for (int r = 9; r < 16; ++r) v[r] = ctw<DIR>(v[r], make_float2(tw[2 * r - 18], tw[2 * r - 17]));
         }
         if constexpr (TC) tc_dft16<DIR>(v, *tc, bar, *tcpar);
-        else dft<16, DIR, PQ>(v);
+        else dft<16, DIR, PQ, FS>(v);
         if constexpr (!last) {
             const int base = (j / Ns) * (16 * Ns) + m;
             if constexpr (Ns % 16 == 0) {
@@ -124,7 +124,7 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ, TC>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ, TC, FS>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
     }
 }
 
@@ -132,8 +132,9 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
 // share the two buffers.  No barrier is needed before the first write: see the buffer rotation
 // above and the callers' barrier placement.  PQ: the quarter-turn form of dft4 (fos_device.cuh).
 // TC: every radix-16 DFT on the tensor cores (fos_tc.cuh; tc and tcpar are then the group's
-// context and MMA-barrier phase, and the tile region may overlap b0 and b1).
-template <int LOGN, int SMAX, bool INV, bool PQ = false, bool TC = false, class Bar>
+// context and MMA-barrier phase, and the tile region may overlap b0 and b1).  FS: the folded
+// second stage of the 16-point DFTs (fos_device.cuh).
+template <int LOGN, int SMAX, bool INV, bool PQ = false, bool TC = false, bool FS = false, class Bar>
 __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
                                        int j, const Bar &bar, const TcCtx *tc = nullptr,
                                        uint32_t *tcpar = nullptr) {
@@ -150,7 +151,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             float2 a[R0];
 #pragma unroll
             for (int r = 0; r < R0; ++r) a[r] = v[q + r * G];
-            dft<R0, DIR, PQ>(a);
+            dft<R0, DIR, PQ, FS>(a);
 #pragma unroll
             for (int r = 0; r < R0; ++r) v[q + r * G] = a[r];
         }
@@ -168,7 +169,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, SMAX, 1, INV, PQ, TC>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
+    fft_tm_pass<LOGN, SMAX, 1, INV, PQ, TC, FS>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
 }
 
 }  // namespace fos

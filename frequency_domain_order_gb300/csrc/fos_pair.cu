@@ -226,7 +226,8 @@ __device__ __forceinline__ void pair_loop(const BlockParams &p, int64_t u, int64
         const int64_t un = u + 1;
         const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, KAPPA, 2);
-        phase_b<8>(p, tlane, g, j, b0, b1, stw, gbar, KAPPA, 2, 32u * (uint32_t)((warp >> 2) & 1));
+        // (the folded 16-point DFT stage: C5 -2.4% measured)
+        phase_b<8, false, true>(p, tlane, g, j, b0, b1, stw, gbar, KAPPA, 2, 32u * (uint32_t)((warp >> 2) & 1));
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
         tmem_fence_after_sync();
