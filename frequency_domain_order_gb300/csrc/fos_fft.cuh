@@ -72,7 +72,7 @@ struct TwLayout {
 // is shifted by NPASS + 1 so that its first write never lands in the buffer the forward
 // transform's last pass reads.  Every buffer is xpad_len(N) elements of this transform.
 
-template <int LOGN, int SMAX, int P, bool INV, bool PQ, bool TC, bool FS, class Bar>
+template <int LOGN, int SMAX, int P, bool INV, bool PQ, bool TC, bool FS, int TWMIN, class Bar>
 __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw,
                                             uint32_t tm, int j, const Bar &bar, const TcCtx *tc,
                                             uint32_t *tcpar) {
@@ -95,11 +95,11 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
         }
         const int m = j & (Ns - 1);
         using TL = TwLayout<LOGN, SMAX>;
-        if constexpr (TL::in_smem(P) && Ns >= 256) {
-            // a pass whose twiddles are all distinct per thread: load W^m, W^{2m}, W^{4m}, W^{8m}
-            // and form the other eleven by products (no power more than three products from the
-            // loaded ones), trading 11 shared-memory loads per thread for 44 FP32 operations
-            // (the two-CTA kernel -1.8%, the resident kernel unchanged; measured)
+        if constexpr (TL::in_smem(P) && Ns >= TWMIN) {
+            // load W^m, W^{2m}, W^{4m}, W^{8m} and form the other eleven twiddles by products (no
+            // power more than three products from the loaded ones): 11 shared-memory loads per
+            // thread traded for 44 FP32 operations, in the passes with Ns >= TWMIN (chosen per
+            // kernel by measurement)
             const float2 *t = stw + TL::smem_off(P) + m;
             float2 w[16];
             w[1] = t[0];
@@ -143,7 +143,7 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
             }
             bar.sync();
         }
-        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ, TC, FS>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
+        fft_tm_pass<LOGN, SMAX, P + 1, INV, PQ, TC, FS, TWMIN>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
     }
 }
 
@@ -152,8 +152,10 @@ __device__ __forceinline__ void fft_tm_pass(float2 (&v)[16], float2 *b0, float2 
 // above and the callers' barrier placement.  PQ: the quarter-turn form of dft4 (fos_device.cuh).
 // TC: every radix-16 DFT on the tensor cores (fos_tc.cuh; tc and tcpar are then the group's
 // context and MMA-barrier phase, and the tile region may overlap b0 and b1).  FS: the folded
-// second stage of the 16-point DFTs (fos_device.cuh).
-template <int LOGN, int SMAX, bool INV, bool PQ = false, bool TC = false, bool FS = false, class Bar>
+// second stage of the 16-point DFTs (fos_device.cuh).  TWMIN: shared-memory passes with Ns >= TWMIN
+// form most of their twiddles by products of four loaded ones.
+template <int LOGN, int SMAX, bool INV, bool PQ = false, bool TC = false, bool FS = false, int TWMIN = 256,
+          class Bar>
 __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, const float2 *stw, uint32_t tm,
                                        int j, const Bar &bar, const TcCtx *tc = nullptr,
                                        uint32_t *tcpar = nullptr) {
@@ -188,7 +190,7 @@ __device__ __forceinline__ void fft_tm(float2 (&v)[16], float2 *b0, float2 *b1, 
             for (int r = 0; r < R0; ++r) wr[xpad((j + q * T) * R0 + r)] = v[q + r * G];
     }
     bar.sync();
-    fft_tm_pass<LOGN, SMAX, 1, INV, PQ, TC, FS>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
+    fft_tm_pass<LOGN, SMAX, 1, INV, PQ, TC, FS, TWMIN>(v, b0, b1, stw, tm, j, bar, tc, tcpar);
 }
 
 }  // namespace fos

@@ -196,9 +196,10 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
         const int64_t un = u + gridDim.x;
         const int chn = un < p.nunits ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < p.nunits && !p.no_bulk) prefetch_window<R_::N, REAL>(p, chan<REAL>(p, chn), lun, tid);
-        // (the packed quarter turn in the P-point transforms: C3 -2.3% measured; the pair kernel
-        // keeps the scalar form, +2.4% otherwise)
-        phase_b<R_::C, true>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
+        // (the packed quarter turn in the P-point transforms: C3 -2.3% measured, the pair kernel
+        // +2.4%; the twiddles of both twiddled passes formed from four loaded ones: C3 -2.4%,
+        // the pair kernel +3.9%)
+        phase_b<R_::C, true, false, 16>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();

@@ -123,7 +123,7 @@ __device__ __forceinline__ void prefetch_window(const BlockParams &p, const Chan
 // Phase B: P-point FFT, multiply by H, inverse FFT for the CL local sub-transforms
 // c' = g, g + 2, ... (Tensor Memory columns 64 c'), whose bins are H[c + C d] with
 // c = hoff + hstride c'.  col0 = 32 (j >> 7), passed in by the caller as a warp-uniform value.
-template <int CL, bool PQ = false, bool FS = false>
+template <int CL, bool PQ = false, bool FS = false, int TWMIN = 256>
 __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
                                         float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar, int hoff,
                                         int hstride, uint32_t col0) {
@@ -143,14 +143,14 @@ __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, in
                 v[8 + e] = make_float2(f1[2 * e], f1[2 * e + 1]);
             }
         }
-        fft_tm<LOGP, 256, false, PQ, false, FS>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, false, PQ, false, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar);
         const float2 *hp = p.H + (hoff + hstride * c) * P + j;
         float2 h[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) h[e] = __ldg(hp + 256 * e);
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], h[e]);
-        fft_tm<LOGP, 256, true, PQ, false, FS>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, true, PQ, false, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar);
         {
             float f0[16], f1[16];
 #pragma unroll
