@@ -714,17 +714,16 @@ int fir_os_plan_create(fir_os_plan_t *out, int M, int N, int data_kind, int coef
                                  stream)) != cudaSuccess)
             return bail(cuda_fail(e, "twiddle upload"));
         if (p->kernel.split_c > 0) {
-            // W_N^{rc} (r < 128, c < C) and W_N^{128 k} (k < N / 128), float64 then rounded
-            const int C = p->kernel.split_c, HI = N / 128;
-            std::vector<float2> twa((size_t)(C * 128 + HI));
-            for (int c = 0; c < C; ++c)
-                for (int r = 0; r < 128; ++r) {
-                    const double ang = -2.0 * M_PI * (double)(r * c) / (double)N;
-                    twa[(size_t)c * 128 + r] = make_float2((float)std::cos(ang), (float)std::sin(ang));
-                }
-            for (int k = 0; k < HI; ++k) {
-                const double ang = -2.0 * M_PI * (double)k / (double)HI;
-                twa[(size_t)C * 128 + k] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            // W_N^b for b = r + 128 m, as its factors: W_N^r (r < 128), then W_N^{128 m} (m < 32);
+            // float64, then rounded
+            std::vector<float2> twa((size_t)(128 + 32));
+            for (int r = 0; r < 128; ++r) {
+                const double ang = -2.0 * M_PI * (double)r / (double)N;
+                twa[(size_t)r] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+            for (int m = 0; m < 32; ++m) {
+                const double ang = -2.0 * M_PI * (double)(128 * m) / (double)N;
+                twa[(size_t)128 + m] = make_float2((float)std::cos(ang), (float)std::sin(ang));
             }
             if ((e = dev_alloc(&p->d_twa, sizeof(float2) * twa.size())) != cudaSuccess)
                 return bail(alloc_fail(e, "cudaMalloc(split twiddles)"));

@@ -14,8 +14,8 @@ struct BlockParams {
     const float2 *H;       // N bins, H / N: natural order, or c-major (H[c + C d] at [c P + d])
                            // for the resident kernel
     const float2 *tw;      // Stockham pass twiddles of the per-CTA transform
-    const float2 *twa;     // resident / pair kernels: W_N^{r c} at [c * 128 + r] (c < C),
-                           // then W_N^{128 k} at [C * 128 + k] (k < N / 128)
+    const float2 *twa;     // resident / pair kernels: W_N^r at [r] (r < 128), then W_N^{128 m}
+                           // at [128 + m] (m < 32): the two factors of W_N^b, b = r + 128 m
     const float2 *btc;     // tensor-core variant: the split 16-point DFT matrices (fos_tc.cuh),
                            // forward hi, forward lo, inverse hi, inverse lo, 4 KB each
     int *err;              // device error word (set to 1 when a bounded wait ran out)

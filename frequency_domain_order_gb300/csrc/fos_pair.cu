@@ -49,15 +49,14 @@ struct PairCfg {
     static constexpr int N = 1 << LOGN;
     static constexpr int P = 4096;
     static constexpr int CL = 8;             // local sub-transforms per CTA
-    static constexpr int HI = N / 128;       // period of W_N^{128 m c} in m c
     static constexpr int THREADS = 512;
     static constexpr int TM_COLS = 512;
     using TL = TwLayout<12, 256>;
     static constexpr int BUF = xpad_len(P);
     static constexpr int OFF_TW = 128;
-    static constexpr int OFF_HI = OFF_TW + 8 * TL::SMEM_ENTRIES;
-    static constexpr int OFF_WR = OFF_HI + 8 * HI;
-    static constexpr int OFF_BUF = (OFF_WR + 8 * 16 * 128 + 127) / 128 * 128;
+    static constexpr int OFF_HI = OFF_TW + 8 * TL::SMEM_ENTRIES;  // W_N^{128 m}, m < 32
+    static constexpr int OFF_WR = OFF_HI + 8 * 32;                 // W_N^r, r < 128
+    static constexpr int OFF_BUF = (OFF_WR + 8 * 128 + 127) / 128 * 128;
     static constexpr int SMEM_BYTES = OFF_BUF + 2 * 2 * 8 * BUF;
     // phase C receive buffer (reuses the exchange buffers): P_other[a'][m mod 16][r]
     static constexpr int RECV_ELEMS = 8 * 16 * 128;
@@ -288,13 +287,13 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
         tmem_relinquish();
     }
     for (int k = tid; k < Q::TL::SMEM_ENTRIES; k += Q::THREADS) stw[k] = p.tw[k];
-    for (int k = tid; k < Q::HI; k += Q::THREADS) hi_s[k] = p.twa[16 * 128 + k];
-    for (int k = tid; k < 16 * 128; k += Q::THREADS) wr_s[k] = p.twa[k];
+    for (int k = tid; k < 32; k += Q::THREADS) hi_s[k] = p.twa[128 + k];
+    for (int k = tid; k < 128; k += Q::THREADS) wr_s[k] = p.twa[k];
     tmem_fence_before_sync();
     cluster_sync();  // both CTAs are running (and set up) before any remote store
     tmem_fence_after_sync();
     const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
-    const float2 wr1 = wr_s[128 + r];  // W_N^r
+    const float2 wr1 = wr_s[r];  // W_N^r
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 

@@ -19,7 +19,8 @@
 //   phase A  thread (s, r) = (t / 128, t mod 128) owns b = r + 128 (8 s + i), i = 0..7.  It
 //            loads xt[blk L - (M-1) + P a + b] for every a (the window was prefetched into L2
 //            while the previous block was being transformed), does the C-point DFTs over a,
-//            multiplies by W_N^{bc} = W_N^{rc} W_{N/128}^{mc} and writes (b, c) to its lane.
+//            multiplies by W_N^{bc} (the powers of W_N^b = W_N^r W_N^{128 m}) and writes (b, c)
+//            to its lane.
 //   phase B  two groups of 256 threads; group g transforms c = g, g + 2, ...  Thread j of a
 //            group holds b = j + 256 e, e = 0..15 (32 contiguous columns of lane j mod 128)
 //            and runs the P-point FFT of fos_fft.cuh (twiddles in shared memory), the
@@ -46,18 +47,17 @@ struct ResidentCfg {
     static constexpr int LOGP = 12;
     static constexpr int P = 1 << LOGP;
     static constexpr int C = N / P;          // 4 or 8
-    static constexpr int HI = N / 128;       // period of W_N^{128 m c} in m c
     static constexpr int THREADS = 512;
     static constexpr int GT = 256;           // threads of one phase-B group
     static constexpr int TM_COLS = 64 * C;   // 32 C complex slots per lane
     using TL = TwLayout<LOGP, 256>;          // every pass twiddle of the P-point FFT in shared memory
     static constexpr int BUF = xpad_len(P);  // elements of one exchange buffer
-    // shared memory: 128-byte header (Tensor Memory address), pass twiddles, W_{N/128}^k,
-    // W_N^{rc}, then two exchange buffers per group
+    // shared memory: 128-byte header (Tensor Memory address), pass twiddles, W_N^{128 m} (m < 32),
+    // W_N^r (r < 128), then two exchange buffers per group
     static constexpr int OFF_TW = 128;
     static constexpr int OFF_HI = OFF_TW + 8 * TL::SMEM_ENTRIES;
-    static constexpr int OFF_WR = OFF_HI + 8 * HI;
-    static constexpr int OFF_BUF = (OFF_WR + 8 * C * 128 + 127) / 128 * 128;
+    static constexpr int OFF_WR = OFF_HI + 8 * 32;
+    static constexpr int OFF_BUF = (OFF_WR + 8 * 128 + 127) / 128 * 128;
     static constexpr int SMEM_BYTES = OFF_BUF + 2 * 2 * 8 * BUF;
     static_assert(C == 4 || C == 8, "N = 16384 or 32768");
     static_assert(TL::SMEM_ENTRIES == FftShape<LOGP>::TW_ENTRIES, "all pass twiddles in shared memory");
@@ -82,7 +82,7 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
     const int lim = p.n - sc > (int64_t)R_::N + p.L ? R_::N + p.L : (int)(p.n - sc);
     const int64_t sa = (REAL ? 2 * ua : ua) * p.L - (p.M - 1);  // xt index of E[0] of unit ua
     const bool interior = sa >= 0 && sa + R_::N + (REAL ? p.L : 0) <= p.n;
-    const float2 wr1 = wr_s[128 + r];  // W_N^r
+    const float2 wr1 = wr_s[r];  // W_N^r
 #pragma unroll 1
     for (int st = 0; st < 4; ++st) {
         const int i0 = (st & 1) + 4 * (st >> 1);  // 0, 1, 4, 5: steps i0 and i0 + 2
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
         tmem_relinquish();
     }
     for (int k = tid; k < R_::TL::SMEM_ENTRIES; k += R_::THREADS) stw[k] = p.tw[k];
-    for (int k = tid; k < R_::HI; k += R_::THREADS) hi_s[k] = p.twa[R_::C * 128 + k];
-    for (int k = tid; k < R_::C * 128; k += R_::THREADS) wr_s[k] = p.twa[k];
+    for (int k = tid; k < 32; k += R_::THREADS) hi_s[k] = p.twa[128 + k];
+    for (int k = tid; k < 128; k += R_::THREADS) wr_s[k] = p.twa[k];
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
