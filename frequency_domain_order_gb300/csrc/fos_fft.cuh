@@ -13,6 +13,13 @@
 // Twiddles for pass p (p >= 1) come from a float32 table (computed in float64 on the host)
 // laid out as tw[twoff(p) + (r-1) * Ns + m] = e^{-2 pi i m r / (16 Ns)}, m = 0..Ns-1, so that
 // consecutive threads read consecutive entries.  The inverse uses their conjugates.
+//
+// Compile-time variants, each chosen per kernel by measurement (the same change sped one kernel
+// up and slowed another): PQ, the quarter-turn form of the radix-4 butterflies; FS, the 16-point
+// DFT's second stage with its sqrt(1/2) factors folded into fused multiply-adds; TWMIN, the
+// smallest Ns at which a shared-memory pass loads 4 of its 15 twiddles and forms the rest by
+// products; TC, the 16-point DFTs on the tensor cores (fos_tc.cuh).  All give results within the
+// same float32 rounding; they differ in instruction mix, not in what is computed.
 #pragma once
 
 #include "fos_device.cuh"
