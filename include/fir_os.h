@@ -215,12 +215,13 @@ int fir_os_plan_set_dft_engine(fir_os_plan_t plan, int engine);
  * and the device buffers of fir_os_plan_create, fir_chan_plan_create and the first
  * fir_os_execute_host call) fail as if memory had run out, without asking CUDA; k = 0
  * disarms.  The failing call returns FIR_OS_E_NOMEM and releases everything it had allocated.
- * A process-wide host-side test hook (not for concurrent use); FIR_OS_E_INVAL for k < 0. */
+ * A process-wide host-side test hook (not for concurrent use) for the library's own error
+ * paths; the claim has no counterpart.  FIR_OS_E_INVAL for k < 0. */
 int fir_os_debug_fail_alloc(int k);
 
 /* fir_os_debug_live_allocs -- the number of the library's allocations (plan objects and device
  * buffers) alive now, process-wide; with fir_os_debug_fail_alloc it shows that a failed call
- * left nothing behind. */
+ * left nothing behind.  A test aid; the claim has no counterpart. */
 int64_t fir_os_debug_live_allocs(void);
 
 /*
