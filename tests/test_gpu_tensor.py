@@ -155,3 +155,24 @@ def test_tensor_engine_batched_channels(fo):
         assert_parity(y[c], want, h, xs[c], f"tensor engine, channel {c}")
         assert np.array_equal(st[c].cpu().numpy(), s_want.astype(np.complex64))
     plan.close()
+
+
+def test_tensor_engine_host_buffers(fo):
+    """The host-buffer entry point with the tensor engine (the kernel reads and writes page-locked
+    memory in place, gathering every window with plain loads) equals the device-buffer call."""
+    import torch
+    w = W.scaled(W.WORKLOADS["C2"], 40, 999)
+    x = W.make_x(w)
+    plan = _tensor_plan(fo, w)
+    y_dev, s_dev = run_calls(plan, x, w.calls)
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    sh = torch.zeros(w.M - 1, dtype=xh.dtype).pin_memory()
+    plan.execute_host(xh, yh, sh)
+    plan.device_status()
+    assert np.array_equal(yh.numpy().view(np.uint32), y_dev.view(np.uint32))
+    assert np.array_equal(sh.numpy(), s_dev)
+    h = W.oracle_h(w)
+    want, _ = oracle.direct(x, h)
+    assert_parity(yh.numpy(), want, h, x, "tensor engine, host buffers")
+    plan.close()
