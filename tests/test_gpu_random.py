@@ -75,9 +75,21 @@ def _filter_case(rng):
             if real:
                 want = want.real
             d = got.astype(np.complex128) - want
-            rel = np.linalg.norm(d) / max(np.linalg.norm(want), 1e-30)
+            # The relative L2 bar is a property of an output vector: the rounding error of an
+            # FFT convolution is absolute, about eps log2(N) ||h||_2 rms(window) per sample, so a
+            # call of one or two outputs whose values happen to lie near zero would be held to
+            # more than float32 holds.  Below 16 outputs the denominator is floored at the size
+            # such outputs have for these inputs, sqrt(n) ||h||_2 rms(window).
+            den = np.linalg.norm(want)
+            if want.size < 16:
+                win = np.concatenate([s0[c], x[c]]) if M > 1 else x[c]
+                rms = np.sqrt(np.mean(np.abs(win.astype(np.complex128)) ** 2))
+                den = max(den, np.sqrt(want.size) * np.linalg.norm(h64) * rms)
+            rel = np.linalg.norm(d) / max(den, 1e-30)
             rt, at = _bar(h64, x[c])
-            assert np.all(np.isfinite(got)) and rel <= rt and np.abs(d).max() <= at, label
+            assert np.all(np.isfinite(got)) and rel <= rt and np.abs(d).max() <= at, (
+                f"{label} channel {c}: finite {np.all(np.isfinite(got))}, rel-L2 {rel:.3g}, "
+                f"max-abs {np.abs(d).max():.3g} (bar {at:.3g})")
         if M > 1:
             assert np.array_equal(s[c], np.concatenate([s0[c], x[c]])[-(M - 1):]), label
 
