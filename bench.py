@@ -871,7 +871,7 @@ def main(argv=None):
                     help="comma-separated further workloads measured in the same run and reported under "
                          f"'also' (default: {','.join(DEFAULT_ALSO)} with the default workload, else none)")
     ap.add_argument("--dft-engine", choices=["fp32", "tensor"], default="fp32",
-                    help="16-point DFTs as float32 butterflies (default) or on the tensor cores (N = 4096 only)")
+                    help="16-point DFTs as float32 butterflies (default) or on the tensor cores (N = 4096 and N >= 16384)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="shorten a single-call workload to this many blocks (smaller profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=50)

@@ -463,7 +463,7 @@ int launch_blocks(fir_os_plan *p, const void *x, int64_t n, void *y, void *state
     // set-up of the plan constants would sit on the call's critical path; the variant that keeps
     // them in shared memory avoids it
     if (p->dft_engine == FIR_OS_DFT_TENSOR) {
-        func = p->kernel.func_tc;
+        func = channels > 1 && p->kernel.func_multi_tc ? p->kernel.func_multi_tc : p->kernel.func_tc;
         cfg.dynamicSmemBytes = (size_t)p->kernel.smem_tc;
     } else if (p->kernel.func_short && bp.nunits < (int64_t)p->max_units_in_flight * p->kernel.groups) {
         func = p->kernel.func_short;
@@ -817,7 +817,8 @@ int fir_os_plan_set_dft_engine(fir_os_plan_t plan, int engine) {
     if (engine != FIR_OS_DFT_FP32 && engine != FIR_OS_DFT_TENSOR)
         return fail(FIR_OS_E_INVAL, "engine %d is neither FIR_OS_DFT_FP32 nor FIR_OS_DFT_TENSOR", engine);
     if (engine == FIR_OS_DFT_TENSOR && !plan->kernel.func_tc)
-        return fail(FIR_OS_E_UNSUPPORTED, "the tensor-core DFT engine exists for N = 4096 only (N = %d)", plan->N);
+        return fail(FIR_OS_E_UNSUPPORTED,
+                    "the tensor-core DFT engine exists for N = 4096, 16384, 32768 and 65536 (N = %d)", plan->N);
     if (engine == FIR_OS_DFT_TENSOR && !plan->d_btc) {
         int rc = check_device(plan);
         if (rc) return rc;
@@ -855,9 +856,10 @@ int fir_os_plan_set_dft_engine(fir_os_plan_t plan, int engine) {
             plan->d_btc = nullptr;
             return cuda_fail(e, "tensor-core DFT matrix upload");
         }
-        if ((e = cudaFuncSetAttribute(plan->kernel.func_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      plan->kernel.smem_tc)) != cudaSuccess)
-            return cuda_fail(e, "cudaFuncSetAttribute(smem, tensor-core variant)");
+        for (const void *f : {plan->kernel.func_tc, plan->kernel.func_multi_tc})
+            if (f && (e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               plan->kernel.smem_tc)) != cudaSuccess)
+                return cuda_fail(e, "cudaFuncSetAttribute(smem, tensor-core variant)");
     }
     plan->dft_engine = engine;
     return FIR_OS_OK;

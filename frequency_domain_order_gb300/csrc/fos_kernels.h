@@ -70,6 +70,7 @@ struct KernelEntry {
     const void *func_short = nullptr;  // the variant for calls of less than one wave, if any
     int smem_short = 0;                // its dynamic shared memory per CTA (bytes)
     const void *func_tc = nullptr;     // the variant with its 16-point DFTs on the tensor cores, if any
+    const void *func_multi_tc = nullptr;  // the tensor-core variant for several channels, if separate
     int smem_tc = 0;                   // its dynamic shared memory per CTA (bytes)
     int threads = 0;             // threads per CTA
     int smem = 0;                // dynamic shared memory per CTA (bytes)

@@ -58,6 +58,13 @@ struct PairCfg {
     static constexpr int OFF_WR = OFF_HI + 8 * 32;                 // W_N^r, r < 128
     static constexpr int OFF_BUF = (OFF_WR + 8 * 128 + 127) / 128 * 128;
     static constexpr int SMEM_BYTES = OFF_BUF + 2 * 2 * 8 * BUF;
+    // the tensor-core variant (as in fos_resident.cu): DFT-matrix tiles after the buffers, one
+    // MMA-completion mbarrier per group in the header, A tiles over the group's exchange buffers
+    static constexpr int OFF_BTC = (SMEM_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_TC = OFF_BTC + 4 * (int)kTcBTileBytes;
+    static constexpr int OFF_TCBAR = 64;
+    static_assert(2 * 8 * BUF >= 4 * (int)kTcTileBytes && SMEM_TC <= 227 * 1024 && OFF_TCBAR + 16 <= OFF_TW,
+                  "tensor-core variant layout");
     // phase C receive buffer (reuses the exchange buffers): P_other[a'][m mod 16][r]
     static constexpr int RECV_ELEMS = 8 * 16 * 128;
     static_assert(8 * RECV_ELEMS <= 2 * 2 * 8 * BUF, "receive buffer inside the exchange buffers");
@@ -208,11 +215,12 @@ __device__ __forceinline__ void pair_phase_c2a(const BlockParams &p, int64_t uc,
 
 // The block loop of CTA KAPPA of a cluster (a copy per rank, so that every rank-dependent choice
 // is made at compile time).
-template <bool REAL, bool MULTI, int KAPPA>
+template <bool REAL, bool MULTI, int KAPPA, bool TC>
 __device__ __forceinline__ void pair_loop(const BlockParams &p, int64_t u, int64_t uend, int tid, int warp, int s,
                                           int r, int g, int j, uint32_t tlane, const float2 *stw,
                                           const float2 *hi_s, float2 wr1, float2 *bufs, float2 *b0, float2 *b1,
-                                          uint32_t peer_recv, const GroupBarrier<256> &gbar) {
+                                          uint32_t peer_recv, const GroupBarrier<256> &gbar, TcCtx *tc,
+                                          uint32_t *tcpar) {
     using Q = PairCfg<REAL>;
     int64_t lu = 0, lun = 0;
     int chu = u < uend ? channel_of<MULTI>(p, u, lu) : 0;  // unit u's channel
@@ -226,7 +234,8 @@ __device__ __forceinline__ void pair_loop(const BlockParams &p, int64_t u, int64
         const int chn = un < uend ? channel_of<MULTI>(p, un, lun) : chu;
         if (un < uend && !p.no_bulk) prefetch_window<Q::N, REAL>(p, chan<REAL>(p, chn), lun, tid, KAPPA, 2);
         // (the folded 16-point DFT stage: C5 -2.4% measured)
-        phase_b<8, false, true>(p, tlane, g, j, b0, b1, stw, gbar, KAPPA, 2, 32u * (uint32_t)((warp >> 2) & 1));
+        phase_b<8, false, true, 256, TC>(p, tlane, g, j, b0, b1, stw, gbar, KAPPA, 2,
+                                         32u * (uint32_t)((warp >> 2) & 1), tc, tcpar);
         tmem_fence_before_sync();
         cluster_sync();  // both CTAs are past phase B (and past every read of S0)
         tmem_fence_after_sync();
@@ -250,7 +259,8 @@ __device__ __forceinline__ void pair_loop(const BlockParams &p, int64_t u, int64
     }
 }
 
-template <bool REAL, bool MULTI>
+// TC: the 4096-point transforms' 16-point DFTs on the tensor cores (the optional engine)
+template <bool REAL, bool MULTI, bool TC = false>
 __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     using Q = PairCfg<REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -289,20 +299,40 @@ __global__ void __launch_bounds__(512, 1) fos_pair_kernel(const BlockParams p) {
     for (int k = tid; k < Q::TL::SMEM_ENTRIES; k += Q::THREADS) stw[k] = p.tw[k];
     for (int k = tid; k < 32; k += Q::THREADS) hi_s[k] = p.twa[128 + k];
     for (int k = tid; k < 128; k += Q::THREADS) wr_s[k] = p.twa[k];
+    uint64_t *tcbar = reinterpret_cast<uint64_t *>(smem + Q::OFF_TCBAR) + g;
+    if constexpr (TC) {  // the split DFT matrices (read by the tensor cores) and the MMA barriers
+        float2 *bt = reinterpret_cast<float2 *>(smem + Q::OFF_BTC);
+        for (int k = tid; k < 4 * (int)kTcBTileBytes / 8; k += Q::THREADS) bt[k] = p.btc[k];
+        fence_proxy_async_smem();
+        if (j == 0) {
+            mbar_init(tcbar, 1);
+            fence_mbar_init();
+        }
+    }
     tmem_fence_before_sync();
     cluster_sync();  // both CTAs are running (and set up) before any remote store
     tmem_fence_after_sync();
     const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
+    TcCtx tc{};
+    uint32_t tcpar = 0u;
+    if constexpr (TC) {
+        tc.a_base = smem_addr(b0);
+        tc.b_base = smem_addr(smem + Q::OFF_BTC);
+        tc.row_off = (uint32_t)(j >> 7) * 2u * kTcTileBytes + tc_offset(j & 127, 0);
+        tc.mbar = tcbar;
+        tc.err = p.err;
+        tc.leader = j == 0;
+    }
     const float2 wr1 = wr_s[r];  // W_N^r
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
     if (kappa == 0)
-        pair_loop<REAL, MULTI, 0>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1, peer_recv,
-                                  gbar);
+        pair_loop<REAL, MULTI, 0, TC>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1,
+                                      peer_recv, gbar, &tc, &tcpar);
     else
-        pair_loop<REAL, MULTI, 1>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1, peer_recv,
-                                  gbar);
+        pair_loop<REAL, MULTI, 1, TC>(p, u, uend, tid, warp, s, r, g, j, tlane, stw, hi_s, wr1, bufs, b0, b1,
+                                      peer_recv, gbar, &tc, &tcpar);
 
     tmem_fence_before_sync();
     __syncthreads();
@@ -316,6 +346,9 @@ KernelEntry pair_entry() {
     KernelEntry k;
     k.func = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, false>);
     k.func_multi = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, true>);
+    k.func_tc = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, false, true>);
+    k.func_multi_tc = reinterpret_cast<const void *>(&fos_pair_kernel<REAL, true, true>);
+    k.smem_tc = Q::SMEM_TC;
     k.threads = Q::THREADS;
     k.smem = Q::SMEM_BYTES;
     k.cluster = 2;

@@ -59,7 +59,15 @@ struct ResidentCfg {
     static constexpr int OFF_WR = OFF_HI + 8 * 32;
     static constexpr int OFF_BUF = (OFF_WR + 8 * 128 + 127) / 128 * 128;
     static constexpr int SMEM_BYTES = OFF_BUF + 2 * 2 * 8 * BUF;
+    // the tensor-core variant: the four 4 KB DFT-matrix tiles after the buffers, and one
+    // MMA-completion mbarrier per group in the header; a group's A tiles (64 KB) overlap its
+    // two exchange buffers
+    static constexpr int OFF_BTC = (SMEM_BYTES + 1023) / 1024 * 1024;
+    static constexpr int SMEM_TC = OFF_BTC + 4 * (int)kTcBTileBytes;
+    static constexpr int OFF_TCBAR = 64;
     static_assert(C == 4 || C == 8, "N = 16384 or 32768");
+    static_assert(2 * 8 * BUF >= 4 * (int)kTcTileBytes && SMEM_TC <= 227 * 1024 && OFF_TCBAR + 16 <= OFF_TW,
+                  "tensor-core variant layout");
     static_assert(TL::SMEM_ENTRIES == FftShape<LOGP>::TW_ENTRIES, "all pass twiddles in shared memory");
 };
 
@@ -142,7 +150,8 @@ __device__ __forceinline__ void phase_ca(const BlockParams &p, int64_t uc, void 
     if (ua >= 0) tmem_wait_st();
 }
 
-template <int LOGN, bool REAL, bool MULTI>
+// TC: the P-point transforms' 16-point DFTs on the tensor cores (the optional engine)
+template <int LOGN, bool REAL, bool MULTI, bool TC = false>
 __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams p) {
     using R_ = ResidentCfg<LOGN, REAL>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -171,10 +180,30 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
     for (int k = tid; k < R_::TL::SMEM_ENTRIES; k += R_::THREADS) stw[k] = p.tw[k];
     for (int k = tid; k < 32; k += R_::THREADS) hi_s[k] = p.twa[128 + k];
     for (int k = tid; k < 128; k += R_::THREADS) wr_s[k] = p.twa[k];
+    uint64_t *tcbar = reinterpret_cast<uint64_t *>(smem + R_::OFF_TCBAR) + g;
+    if constexpr (TC) {  // the split DFT matrices (read by the tensor cores) and the MMA barriers
+        float2 *bt = reinterpret_cast<float2 *>(smem + R_::OFF_BTC);
+        for (int k = tid; k < 4 * (int)kTcBTileBytes / 8; k += R_::THREADS) bt[k] = p.btc[k];
+        fence_proxy_async_smem();
+        if (j == 0) {
+            mbar_init(tcbar, 1);
+            fence_mbar_init();
+        }
+    }
     tmem_fence_before_sync();
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tlane = __shfl_sync(0xffffffffu, *tm_slot, 0) + ((uint32_t)(32 * (warp & 3)) << 16);
+    TcCtx tc{};
+    uint32_t tcpar = 0u;
+    if constexpr (TC) {
+        tc.a_base = smem_addr(b0);
+        tc.b_base = smem_addr(smem + R_::OFF_BTC);
+        tc.row_off = (uint32_t)(j >> 7) * 2u * kTcTileBytes + tc_offset(j & 127, 0);
+        tc.mbar = tcbar;
+        tc.err = p.err;
+        tc.leader = j == 0;
+    }
     // the set-up read plan memory only; x, y and the state may belong to the previous kernel
     griddep_wait();
 
@@ -199,7 +228,8 @@ __global__ void __launch_bounds__(512, 1) fos_resident_kernel(const BlockParams 
         // (the packed quarter turn in the P-point transforms: C3 -2.3% measured, the pair kernel
         // +2.4%; the twiddles of both twiddled passes formed from four loaded ones: C3 -2.4%,
         // the pair kernel +3.9%)
-        phase_b<R_::C, true, false, 16>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1));
+        phase_b<R_::C, true, false, 16, TC>(p, tlane, g, j, b0, b1, stw, gbar, 0, 1, 32u * (uint32_t)((warp >> 2) & 1),
+                                            &tc, &tcpar);
         tmem_fence_before_sync();
         __syncthreads();  // every c has been filtered
         tmem_fence_after_sync();
@@ -222,6 +252,9 @@ KernelEntry resident_entry() {
     KernelEntry k;
     k.func = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, false>);
     k.func_multi = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, true>);
+    k.func_tc = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, false, true>);
+    k.func_multi_tc = reinterpret_cast<const void *>(&fos_resident_kernel<LOGN, REAL, true, true>);
+    k.smem_tc = R_::SMEM_TC;
     k.threads = R_::THREADS;
     k.smem = R_::SMEM_BYTES;
     k.cluster = 1;

@@ -123,14 +123,23 @@ __device__ __forceinline__ void prefetch_window(const BlockParams &p, const Chan
 // Phase B: P-point FFT, multiply by H, inverse FFT for the CL local sub-transforms
 // c' = g, g + 2, ... (Tensor Memory columns 64 c'), whose bins are H[c + C d] with
 // c = hoff + hstride c'.  col0 = 32 (j >> 7), passed in by the caller as a warp-uniform value.
-template <int CL, bool PQ = false, bool FS = false, int TWMIN = 256>
+// TC: the 16-point DFTs of the P-point transforms on the tensor cores (fos_tc.cuh).  Their
+// accumulators are the sub-transform's own 64 columns, free while its values are in registers:
+// tile t (the vectors of threads j = 128 t .. 128 t + 127) at columns 64 c' + 32 t of every lane,
+// so thread j reads its DFT back from its own columns.  tc->a_base, b_base, row_off, mbar, err and
+// leader are set by the caller (the A tiles overlap b0 and b1).
+template <int CL, bool PQ = false, bool FS = false, int TWMIN = 256, bool TC = false>
 __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, int g, int j, float2 *b0,
                                         float2 *b1, const float2 *stw, const GroupBarrier<256> &gbar, int hoff,
-                                        int hstride, uint32_t col0) {
+                                        int hstride, uint32_t col0, TcCtx *tc = nullptr, uint32_t *tcpar = nullptr) {
     constexpr int LOGP = 12, P = 1 << LOGP;
 #pragma unroll 1
     for (int c = g; c < CL; c += 2) {
         const uint32_t ta = tlane + 64u * (uint32_t)c + col0;
+        if constexpr (TC) {
+            tc->d_row = ta;
+            tc->d_tile = (tlane & 0xFFFFu) + 64u * (uint32_t)c;  // lane 0, the sub-transform's first column
+        }
         float2 v[16];
         {
             float f0[16], f1[16];
@@ -143,14 +152,14 @@ __device__ __forceinline__ void phase_b(const BlockParams &p, uint32_t tlane, in
                 v[8 + e] = make_float2(f1[2 * e], f1[2 * e + 1]);
             }
         }
-        fft_tm<LOGP, 256, false, PQ, false, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, false, PQ, TC, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar, tc, tcpar);
         const float2 *hp = p.H + (hoff + hstride * c) * P + j;
         float2 h[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) h[e] = __ldg(hp + 256 * e);
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = cmul(v[e], h[e]);
-        fft_tm<LOGP, 256, true, PQ, false, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar);
+        fft_tm<LOGP, 256, true, PQ, TC, FS, TWMIN>(v, b0, b1, stw, 0u, j, gbar, tc, tcpar);
         {
             float f0[16], f1[16];
 #pragma unroll

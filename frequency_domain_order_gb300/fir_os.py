@@ -222,7 +222,7 @@ class Plan:
         _check(lib().fir_os_device_status(self._h, _stream_handle(stream)))
 
     def set_dft_engine(self, engine: int):
-        """fir_os_plan_set_dft_engine: DFT_FP32 (default) or DFT_TENSOR (N = 4096 only)."""
+        """fir_os_plan_set_dft_engine: DFT_FP32 (default) or DFT_TENSOR (N = 4096 and N >= 16384)."""
         _check(lib().fir_os_plan_set_dft_engine(self._h, int(engine)))
 
     def set_wait_limit(self, limit_ns: int):

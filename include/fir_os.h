@@ -201,8 +201,9 @@ int fir_os_plan_set_wait_limit(fir_os_plan_t plan, int64_t limit_ns);
  *   FIR_OS_DFT_TENSOR  as matrix products on the tensor cores: 128 vectors per tcgen05.mma tile,
  *                      TF32 operands split into a TF32 part and the float32 rest (three products,
  *                      float32 accumulation in Tensor Memory), the twiddles still in float32.
- * The tensor engine exists for N = 4096 only (FIR_OS_E_UNSUPPORTED otherwise); it is an
- * option, off by default.  Its outputs meet the same parity bar but are not bitwise equal to
+ * The tensor engine exists for N = 4096 (every pass of the block transform) and for N = 16384,
+ * 32768 and 65536 (every pass of their 4096-point sub-transforms; FIR_OS_E_UNSUPPORTED for the
+ * other sizes); it is an option, off by default.  Its outputs meet the same parity bar but are not bitwise equal to
  * the default's.  The first
  * FIR_OS_DFT_TENSOR call allocates and uploads the 16 KB of split DFT matrices (synchronous;
  * FIR_OS_E_NOMEM if that allocation fails).  Applies to launches enqueued after the call.

@@ -1,11 +1,13 @@
 """The tensor-core DFT engine (fir_os_plan_set_dft_engine, FIR_OS_DFT_TENSOR) against the oracle.
 
-With it every radix-16 pass of the N = 4096 block transforms (step 4 of the claim in
+With it every radix-16 pass of the 4096-point transforms (step 4 of the claim in
 "一种基于GPU的高阶数字FIR滤波器频域并行处理实现方法", 主权项) computes its 16-point DFTs as
-tcgen05.mma matrix products on split TF32 operands.  The outputs must meet the same parity bar
-as the float32 engine (relative L2 error <= 1e-5, max abs error <= 1e-4 * ||h||_1 * max|x|,
-measured in float64): whole streams with ragged tails, several calls with the state carried,
-complex and packed real data, the full C2 workload sampled, and M = 1 and M = N.
+tcgen05.mma matrix products on split TF32 operands: the whole block transform at N = 4096, and
+the 4096-point sub-transforms of the N = 16384 / 32768 (one SM) and N = 65536 (two-CTA cluster)
+kernels.  The outputs must meet the same parity bar as the float32 engine (relative L2 error
+<= 1e-5, max abs error <= 1e-4 * ||h||_1 * max|x|, measured in float64): whole streams with
+ragged tails, several calls with the state carried, complex and packed real data, banks of
+channels, the full C2, C3 and C5 workloads sampled, and M = 1 and M = N.
 """
 import numpy as np
 import pytest
@@ -97,8 +99,9 @@ def test_tensor_engine_full_c2_sampled_and_close_to_fp32(fo):
     plan.close()
 
 
-def test_tensor_engine_only_for_4096(fo):
-    for name in ("C1", "C3"):
+def test_tensor_engine_sizes(fo):
+    """Only N = 4096 and N >= 16384 have a tensor-core variant; the others refuse it."""
+    for name in ("C1", "C4"):
         plan = make_plan(W.scaled(W.WORKLOADS[name], 2))
         with pytest.raises(fo.FirOsError) as err:
             plan.set_dft_engine(fo.DFT_TENSOR)
@@ -175,4 +178,91 @@ def test_tensor_engine_host_buffers(fo):
     h = W.oracle_h(w)
     want, _ = oracle.direct(x, h)
     assert_parity(yh.numpy(), want, h, x, "tensor engine, host buffers")
+    plan.close()
+
+
+# the resident (N = 16384, 32768) and two-CTA (N = 65536) kernels: C3's and C5's filters, and the
+# same sizes with real data and with other tap counts
+LARGE = [("C3", False, None, None), ("C5", False, None, None), ("C3", True, None, None), ("C5", True, None, None),
+         ("N16384", False, 16384, 4097), ("N16384", True, 16384, 8193), ("N65536", False, 65536, 1)]
+
+
+def _large_workload(name, real, N, M):
+    if N is None:
+        base = W.WORKLOADS[name]
+        if real:  # the workload's sizes on real data, with real taps
+            base = W.Workload(name + "real", True, base.M, base.N, base.calls, 13, "time", "hamming_lowpass", (0.2,))
+        return base
+    if M == 1:
+        return W.Workload(name, real, M, N, (1,), 17, "time", "complex_normal", (), h_seed=21)
+    return W.Workload(name, real, M, N, (1,), 17, "time", "hamming_lowpass", (0.25,))
+
+
+@pytest.mark.parametrize("name,real,N,M", LARGE)
+@pytest.mark.parametrize("blocks,tail,calls", [(1, 0, 1), (5, 777, 3)])
+def test_tensor_engine_large_transforms(fo, name, real, N, M, blocks, tail, calls):
+    w = W.scaled(_large_workload(name, real, N, M), blocks, tail, calls)
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    plan = _tensor_plan(fo, w)
+    y, st = run_calls(plan, x, w.calls)
+    plan.device_status()
+    if w.n * w.M <= 3e8:
+        want, s_want = oracle.direct(x, h)
+        assert_parity(y, want, h, x, f"{w.name} tensor engine")
+    else:
+        idx = W.sample_indices(w.n, w.L, seed=blocks, n_random=1 << 12, whole_blocks=[0])
+        want = oracle.direct_at(x, h, None, idx)
+        assert_parity(y[idx], want, h, x, f"{w.name} tensor engine, sampled")
+        s_want = oracle.state_next(x, None, w.M)
+    if w.M > 1:
+        assert np.array_equal(st, (s_want.real if real else s_want).astype(st.dtype))
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["C3", "C5"])
+def test_tensor_engine_full_size_sampled(fo, name):
+    """The full C3 / C5 call with the tensor engine, sampled against the oracle, and within the
+    bar of the float32 engine over every output."""
+    w = W.WORKLOADS[name]
+    x = W.make_x(w)
+    h = W.oracle_h(w)
+    xd = to_dev(x)
+    plan = make_plan(w)
+    y32, _ = run_device(plan, xd, w.calls)
+    plan.set_dft_engine(fo.DFT_TENSOR)
+    ytc, _ = run_device(plan, xd, w.calls)
+    plan.device_status()
+    idx = W.sample_indices(w.n, w.L, seed=7, n_random=1 << 13, whole_blocks=[0, w.n // w.L - 1])
+    want = oracle.direct_at(x, h, None, idx)
+    got = ytc.cpu().numpy()
+    assert_parity(got[idx], want, h, x, f"{name} tensor engine, sampled")
+    assert_parity(got, y32.cpu().numpy(), h, x, f"{name}: tensor vs float32 engine")
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["C3", "C5"])
+def test_tensor_engine_large_batched(fo, name):
+    """A bank of three channels through the multi-channel tensor-core variants, two calls."""
+    import torch
+    w = W.scaled(W.WORKLOADS[name], 3, 4321)
+    channels = 3
+    xs = [W.make_x(W.dataclasses.replace(w, x_seed=w.x_seed + 1000 * c)) for c in range(channels)]
+    h = W.oracle_h(w)
+    plan = _tensor_plan(fo, w)
+    xd = torch.stack([to_dev(x) for x in xs])
+    yd = torch.empty_like(xd)
+    st = torch.zeros((channels, w.M - 1), dtype=xd.dtype, device="cuda")
+    half = w.L + 1000
+    plan.execute_batched(xd[:, :half], yd[:, :half], st)
+    plan.execute_batched(xd[:, half:], yd[:, half:], st)
+    torch.cuda.synchronize()
+    plan.device_status()
+    y = yd.cpu().numpy()
+    for c in range(channels):
+        idx = W.sample_indices(w.n, w.L, seed=c, n_random=1 << 12, whole_blocks=[0])
+        want = oracle.direct_at(xs[c], h, None, idx)
+        assert_parity(y[c][idx], want, h, xs[c], f"{name} tensor engine, channel {c}")
+        s_want = oracle.state_next(xs[c], None, w.M)
+        assert np.array_equal(st[c].cpu().numpy(), s_want.astype(np.complex64))
     plan.close()
