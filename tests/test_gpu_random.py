@@ -2,7 +2,7 @@
 real and complex data (real or complex taps), degenerate and random filter lengths, stream
 lengths from empty to many waves of the GPU, streams cut into several calls, banks of channels,
 channelizer banks of every supported K with hops that divide K or not, and the optional
-tensor-core DFT engine on half of the N = 4096 plans.
+tensor-core DFT engine on half of the plans that have it (N = 4096 and N >= 16384).
 
 Each case checks the parity bar (rel-L2 <= 1e-5, max-abs <= 1e-4 ||h||_1 max|x|; sampled outputs
 when the full oracle would be slow; for fewer than 16 outputs the relative bar's denominator is
@@ -63,7 +63,7 @@ def _filter_case(rng):
     x = np.stack([sig(n) for _ in range(channels)])
     s0 = np.stack([sig(M - 1) for _ in range(channels)])
     plan = fir_os.Plan(M, N, torch.from_numpy(h32).cuda(), real=real)
-    tensor = N == 4096 and bool(rng.integers(0, 2))  # the optional tensor-core DFT engine
+    tensor = (N == 4096 or N >= 16384) and bool(rng.integers(0, 2))  # the optional tensor-core DFT engine
     if tensor:
         plan.set_dft_engine(fir_os.DFT_TENSOR)
     xd = torch.from_numpy(x).cuda()
@@ -130,6 +130,9 @@ def _host_case(rng):
     xs = [sig(n), sig(int(rng.integers(0, 3 * span)))]
     s0 = sig(M - 1)
     plan = fir_os.Plan(M, N, torch.from_numpy(h32).cuda(), real=real)
+    tensor = (N == 4096 or N >= 16384) and bool(rng.integers(0, 2))  # the optional tensor-core DFT engine
+    if tensor:
+        plan.set_dft_engine(fir_os.DFT_TENSOR)
     sh = torch.from_numpy(s0.copy())
     if pinned:
         sh = sh.pin_memory()
@@ -144,7 +147,7 @@ def _host_case(rng):
     plan.device_status()
     plan.close()
     label = (f"host N={N} M={M} n={[x.size for x in xs]} real={real} complex-h={hc} "
-             f"{'page-locked' if pinned else 'pageable'}")
+             f"{'page-locked' if pinned else 'pageable'}{' tensor-core DFTs' if tensor else ''}")
     # the two calls are one stream: the oracle filters their concatenation
     x = np.concatenate(xs)
     y = np.concatenate(ys)
